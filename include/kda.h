@@ -1,0 +1,129 @@
+/*
+ * kda.h — C ABI of the KDA (Kimi Delta Attention) chunked-prefill forward
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * The operation (source: "在 TPU 上加速 Kimi K3 KDA", junyi.dev tpu-kda report,
+ * §1–§2 for the recurrence, §4 and §6.2 for the chunked form, §6.5 for the
+ * per-sequence state carry):
+ *
+ *   for every sequence n (tokens cu_seqlens[n] .. cu_seqlens[n+1]-1) and head h,
+ *   with S the [K,V] state (row = key channel) starting at initial_state[n,h]:
+ *       S_t = (I - beta_t k_t k_t^T) Diag(exp g_t) S_{t-1} + beta_t k_t v_t^T
+ *       o_t = scale * S_t^T q_t
+ *   and final_state[n,h] = S after the sequence's last token.
+ *
+ * The library computes it chunk by chunk (64-token chunks, 16-token
+ * sub-blocks): per-chunk gate prefix sum, sub-block-midpoint strip products
+ * for the decayed score matrices, a blocked 16x16 solve with (I+L), the WY
+ * form, then the inter-chunk state recurrence fused with the output. The
+ * sub-block products are safe in bf16 because lower_bound <= g <= 0 bounds
+ * every factor by 2^(8*|lower_bound|/ln 2) (= 2^57.7 at lower_bound = -5,
+ * §4 and §13).
+ *
+ * General contract
+ *   - Every pointer argument is CUDA device memory owned by the caller
+ *     (except where stated). The library allocates nothing per call and keeps
+ *     no state between calls; calls are thread-safe.
+ *   - Calls are asynchronous on `stream`. Argument errors detected on the host
+ *     are returned synchronously and nothing is launched. Data errors detected
+ *     on the device are written to *status_dev (when given); the outputs are
+ *     then unspecified.
+ *   - Results are deterministic: the same inputs give bitwise-equal outputs.
+ */
+#ifndef KDA_GB300_KDA_H
+#define KDA_GB300_KDA_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; 0 (NULL) is the legacy default stream. */
+typedef struct CUstream_st *kda_stream_t;
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = 1, /* null required pointer, bad size, misalignment, bad scalar */
+    KDA_ERR_UNSUPPORTED = 2, /* head_dim_k or head_dim_v other than 128 */
+    KDA_ERR_CUDA = 3,        /* a CUDA runtime call or the launch failed */
+    KDA_ERR_GATE_RANGE = 4,  /* device: some g outside [lower_bound, 0] or not finite */
+    KDA_ERR_BAD_SEQLENS = 5, /* device: cu_seqlens not 0 .. total_tokens nondecreasing */
+    KDA_ERR_TIMEOUT = 6,     /* device: a bounded wait inside a kernel gave up */
+    KDA_ERR_VALUE_RANGE = 7  /* device: a value entering an fp16 tensor-core operand
+                                exceeded 6e4 in magnitude (or was not finite) */
+} kda_status_t;
+
+#define KDA_HEAD_DIM 128
+#define KDA_CHUNK 64
+#define KDA_SUBBLOCK 16
+
+/*
+ * kda_chunk_fwd — KDA chunked prefill forward over varlen-packed sequences.
+ *
+ * Defined by the recurrence above (report §1–§2, §13) computed in the chunked
+ * form of §4 and §6.2, with the state restarting per sequence (§6.5).
+ *
+ * Inputs (device memory, row-major, contiguous):
+ *   q, k          bf16 [total_tokens, num_heads, 128]; k is expected to be
+ *                 L2-normalised per (token, head) as in the model (not checked).
+ *   v             bf16 [total_tokens, num_heads, 128].
+ *   g             fp32 [total_tokens, num_heads, 128]: natural-log decay per
+ *                 key channel, already activated; lower_bound <= g <= 0.
+ *   beta          fp32 [total_tokens, num_heads].
+ *   cu_seqlens    int32 [num_seqs + 1]: cu[0] = 0, nondecreasing,
+ *                 cu[num_seqs] = total_tokens. Empty sequences are allowed.
+ *   initial_state fp32 [num_seqs, num_heads, 128, 128] (S[i][j], i = key
+ *                 channel, j = value channel), or NULL for zeros.
+ *   scale         multiplies o only (typically 128^-0.5).
+ *   lower_bound   the gate's lower bound; must lie in [-10.9, 0] so that the
+ *                 sub-block factors stay below 2^126.
+ * Outputs:
+ *   o             fp32 [total_tokens, num_heads, 128]. (fp32 rather than bf16: a
+ *                 bf16 o alone would round the largest outputs by up to 2^-9 of
+ *                 their magnitude, several percent of the output RMS for the
+ *                 heavy-tailed outputs of this operation.)
+ *   final_state   fp32 [num_seqs, num_heads, 128, 128], or NULL (not written).
+ *                 It may be the same pointer as initial_state (updated in
+ *                 place); any other overlap between outputs and inputs is
+ *                 undefined.
+ *   status_dev    optional device int32: set to 0 on the stream before the
+ *                 launch, then to the first device-detected error code
+ *                 (KDA_ERR_GATE_RANGE, KDA_ERR_BAD_SEQLENS, KDA_ERR_TIMEOUT,
+ *                 KDA_ERR_VALUE_RANGE).
+ *                 A chain whose sequence bounds are invalid is skipped, so no
+ *                 access leaves the given buffers.
+ * Alignment: q, k, v, g, o, initial_state, final_state 16-byte aligned;
+ *   beta, cu_seqlens, status_dev 4-byte aligned.
+ * Precision: products run on tensor cores with fp32 accumulation. The Aqk
+ *   strip operands are split into two bf16 terms (bf16's exponent range holds
+ *   the 2^57.7 factors, the split keeps ~16 significant bits); the Akk strips
+ *   use bf16; the solve, WY form, state recurrence and output products use
+ *   fp16 operands. The state stays fp32 across the whole sequence. Inputs must
+ *   keep |v|, |initial_state| and the state below ~6e4 (fp16 operand range);
+ *   otherwise KDA_ERR_VALUE_RANGE is reported.
+ * Returns KDA_OK once the work is queued, or a host-side error code with
+ * nothing launched. num_seqs == 0 launches nothing.
+ */
+kda_status_t kda_chunk_fwd(const void *q, const void *k, const void *v, const float *g,
+                           const float *beta, const int32_t *cu_seqlens, int32_t num_seqs,
+                           int64_t total_tokens, int32_t num_heads, int32_t head_dim_k,
+                           int32_t head_dim_v, const float *initial_state, float scale,
+                           float lower_bound, float *o, float *final_state,
+                           int32_t *status_dev, kda_stream_t stream);
+
+/* Number of kernel launches one kda_chunk_fwd call makes for these sizes
+ * (0 when num_seqs == 0). Host-only, no CUDA call. */
+int32_t kda_chunk_fwd_launches(int32_t num_seqs, int64_t total_tokens, int32_t num_heads);
+
+/* Static description of an error code; never NULL. */
+const char *kda_status_string(int32_t status);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int32_t kda_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_GB300_KDA_H */

@@ -1,0 +1,159 @@
+"""ctypes binding of ``libkda.so`` (C ABI in ``include/kda.h``).
+
+Argument marshalling only: tensors are checked for dtype, device, shape and
+contiguity and turned into raw pointers; every step of the computation runs
+in the library's CUDA kernels. There is no fallback: if the library is
+missing or fails to load, these functions raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+KDA_OK = 0
+KDA_ERR_INVALID_ARG = 1
+KDA_ERR_UNSUPPORTED = 2
+KDA_ERR_CUDA = 3
+KDA_ERR_GATE_RANGE = 4
+KDA_ERR_BAD_SEQLENS = 5
+KDA_ERR_TIMEOUT = 6
+KDA_ERR_VALUE_RANGE = 7
+
+HEAD_DIM = 128
+EXPORTED = ("kda_chunk_fwd", "kda_chunk_fwd_launches", "kda_status_string", "kda_version")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class KdaError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {status_string(code)} (code {code})")
+        self.code = code
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
+    """Load ``libkda.so``; raises ``OSError`` if it is absent (no fallback)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            if not build_if_missing:
+                raise OSError(f"{path} not found: build it with kda_chunked_prefill_gb300.build.build()")
+            _build.build()
+        lib = ctypes.CDLL(path)
+        vp, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+        lib.kda_chunk_fwd.argtypes = [vp, vp, vp, vp, vp, vp, i32, i64, i32, i32, i32, vp, f32, f32,
+                                      vp, vp, vp, vp]
+        lib.kda_chunk_fwd.restype = ctypes.c_int
+        lib.kda_chunk_fwd_launches.argtypes = [i32, i64, i32]
+        lib.kda_chunk_fwd_launches.restype = i32
+        lib.kda_status_string.argtypes = [i32]
+        lib.kda_status_string.restype = ctypes.c_char_p
+        lib.kda_version.argtypes = []
+        lib.kda_version.restype = i32
+        _lib = lib
+        return lib
+
+
+def status_string(code: int) -> str:
+    return load_library().kda_status_string(int(code)).decode()
+
+
+def version() -> int:
+    return int(load_library().kda_version())
+
+
+def chunk_fwd_launches(num_seqs: int, total_tokens: int, num_heads: int) -> int:
+    return int(load_library().kda_chunk_fwd_launches(int(num_seqs), int(total_tokens), int(num_heads)))
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check(t, name, dtype, shape, device):
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.device != device:
+        raise ValueError(f"{name} must be on {device}, got {t.device}")
+
+
+def kda_chunk_fwd(q, k, v, g, beta, cu_seqlens, initial_state, scale: float, lower_bound: float,
+                  o, final_state, status=None, stream=None) -> int:
+    """Call the C entry point ``kda_chunk_fwd`` with caller-allocated outputs.
+
+    q, k, v: bf16 [T,H,128]; o: fp32 [T,H,128]; g: fp32 [T,H,128]; beta: fp32 [T,H];
+    cu_seqlens: int32 [N+1]; initial_state / final_state: fp32 [N,H,128,128]
+    or None; status: int32 [1] or None. All on one CUDA device. ``stream`` is a
+    ``torch.cuda.Stream`` (default: the current stream). Raises ``KdaError`` on a
+    host-side error; returns ``KDA_OK`` once the work is queued.
+    """
+    T, H, D = q.shape
+    N = cu_seqlens.shape[0] - 1
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    _check(q, "q", torch.bfloat16, (T, H, D), dev)
+    _check(k, "k", torch.bfloat16, (T, H, D), dev)
+    _check(v, "v", torch.bfloat16, (T, H, v.shape[2]), dev)
+    _check(g, "g", torch.float32, (T, H, D), dev)
+    _check(beta, "beta", torch.float32, (T, H), dev)
+    _check(cu_seqlens, "cu_seqlens", torch.int32, (N + 1,), dev)
+    _check(o, "o", torch.float32, tuple(v.shape), dev)
+    if initial_state is not None:
+        _check(initial_state, "initial_state", torch.float32, (N, H, D, v.shape[2]), dev)
+    if final_state is not None:
+        _check(final_state, "final_state", torch.float32, (N, H, D, v.shape[2]), dev)
+    if status is not None:
+        _check(status, "status", torch.int32, (1,), dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    rc = load_library().kda_chunk_fwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), N, T, H, D, v.shape[2],
+        _ptr(initial_state), float(scale), float(lower_bound), _ptr(o), _ptr(final_state),
+        _ptr(status), ctypes.c_void_p(stream.cuda_stream))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_chunk_fwd")
+    return rc
+
+
+def chunk_fwd(q, k, v, g, beta, cu_seqlens, initial_state=None, scale: Optional[float] = None,
+              lower_bound: float = -5.0, output_final_state: bool = True, check: bool = False,
+              stream=None):
+    """Allocate ``o`` (and ``final_state``) and run ``kda_chunk_fwd``.
+
+    Returns ``(o, final_state)``; ``final_state`` is None when not requested.
+    With ``check=True`` the device status word is read back (a synchronising
+    copy) and a device-detected error raises ``KdaError``.
+    """
+    T, H, D = q.shape
+    N = cu_seqlens.shape[0] - 1
+    if scale is None:
+        scale = D ** -0.5
+    o = torch.empty((T, H, v.shape[2]), dtype=torch.float32, device=q.device)
+    fs = (torch.empty((N, H, D, v.shape[2]), dtype=torch.float32, device=q.device)
+          if output_final_state else None)
+    status = torch.zeros(1, dtype=torch.int32, device=q.device) if check else None
+    kda_chunk_fwd(q, k, v, g, beta, cu_seqlens, initial_state, scale, lower_bound, o, fs, status, stream)
+    if check:
+        code = int(status.item())
+        if code != KDA_OK:
+            raise KdaError(code, "kda_chunk_fwd (device)")
+    return o, fs

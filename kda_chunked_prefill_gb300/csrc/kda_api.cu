@@ -1,0 +1,85 @@
+// Host side of the C ABI declared in include/kda.h: argument validation,
+// status zeroing and the launch of the chunked-prefill kernel.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kda.h"
+
+namespace kda {
+namespace chain_mma {
+cudaError_t launch(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                   const int32_t *cu_seqlens, int32_t num_seqs, int64_t total_tokens, int32_t H,
+                   const float *initial_state, float scale, float lower_bound, float *o,
+                   float *final_state, int32_t *status, cudaStream_t stream);
+}
+}  // namespace kda
+
+namespace {
+
+constexpr int32_t kVersion = 100;  // 0.1.0
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// The strip products form factors up to 2^(8*|lower_bound|/ln 2); keep that
+// below 2^126 so they stay finite in bf16 and fp32.
+bool lower_bound_ok(float lb) { return lb >= -10.9f && lb <= 0.0f; }
+
+}  // namespace
+
+extern "C" {
+
+kda_status_t kda_chunk_fwd(const void *q, const void *k, const void *v, const float *g,
+                           const float *beta, const int32_t *cu_seqlens, int32_t num_seqs,
+                           int64_t total_tokens, int32_t num_heads, int32_t head_dim_k,
+                           int32_t head_dim_v, const float *initial_state, float scale,
+                           float lower_bound, float *o, float *final_state,
+                           int32_t *status_dev, kda_stream_t stream) {
+    if (head_dim_k != KDA_HEAD_DIM || head_dim_v != KDA_HEAD_DIM) return KDA_ERR_UNSUPPORTED;
+    if (num_seqs < 0 || total_tokens < 0 || num_heads < 1) return KDA_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(num_seqs) * num_heads > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
+    if (total_tokens > (int64_t{1} << 40) / (static_cast<int64_t>(num_heads) * KDA_HEAD_DIM))
+        return KDA_ERR_INVALID_ARG;
+    if (!(scale == scale) || !lower_bound_ok(lower_bound)) return KDA_ERR_INVALID_ARG;
+    if (num_seqs == 0) return total_tokens == 0 ? KDA_OK : KDA_ERR_INVALID_ARG;
+    if (!cu_seqlens || !aligned(cu_seqlens, 4)) return KDA_ERR_INVALID_ARG;
+    if (total_tokens > 0) {
+        if (!q || !k || !v || !g || !beta || !o) return KDA_ERR_INVALID_ARG;
+        if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(g, 16) ||
+            !aligned(o, 16) || !aligned(beta, 4))
+            return KDA_ERR_INVALID_ARG;
+    }
+    if ((initial_state && !aligned(initial_state, 16)) || (final_state && !aligned(final_state, 16)) ||
+        (status_dev && !aligned(status_dev, 4)))
+        return KDA_ERR_INVALID_ARG;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (status_dev && cudaMemsetAsync(status_dev, 0, sizeof(int32_t), s) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    const cudaError_t e = kda::chain_mma::launch(q, k, v, g, beta, cu_seqlens, num_seqs, total_tokens,
+                                                 num_heads, initial_state, scale, lower_bound, o,
+                                                 final_state, status_dev, s);
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+int32_t kda_chunk_fwd_launches(int32_t num_seqs, int64_t total_tokens, int32_t num_heads) {
+    (void)total_tokens;
+    return (num_seqs > 0 && num_heads > 0) ? 1 : 0;
+}
+
+const char *kda_status_string(int32_t status) {
+    switch (status) {
+        case KDA_OK: return "ok";
+        case KDA_ERR_INVALID_ARG: return "invalid argument";
+        case KDA_ERR_UNSUPPORTED: return "unsupported head dimension (only 128 is built)";
+        case KDA_ERR_CUDA: return "CUDA runtime or launch error";
+        case KDA_ERR_GATE_RANGE: return "gate g outside [lower_bound, 0] or not finite";
+        case KDA_ERR_BAD_SEQLENS: return "cu_seqlens not nondecreasing from 0 to total_tokens";
+        case KDA_ERR_TIMEOUT: return "a bounded wait inside a kernel gave up";
+        case KDA_ERR_VALUE_RANGE: return "a value entering an fp16 tensor-core operand exceeded 6e4 or was not finite";
+        default: return "unknown status";
+    }
+}
+
+int32_t kda_version(void) { return kVersion; }
+
+}  // extern "C"

@@ -1,0 +1,86 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports
+every function ``include/kda.h`` declares, and rejects bad arguments on the
+host before any CUDA call. Runs with ``-m "not gpu"``."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import kda_chunked_prefill_gb300 as kda
+from kda_chunked_prefill_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kda.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"\b([a-z_][a-z0-9_]*)\s*\(", text)
+    keywords = {"if", "sizeof", "defined"}
+    return sorted({n for n in names if n.startswith("kda_") and n not in keywords})
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return _lib.load_library(build_if_missing=True)
+
+
+def test_header_declares_the_documented_entry_points():
+    assert set(_lib.EXPORTED) <= set(declared_functions())
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", _lib.library_path()], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for name in declared_functions():
+        assert name in exported, f"{name} declared in kda.h but not exported"
+        getattr(lib, name)  # resolvable through ctypes
+
+
+def test_version_and_status_strings(lib):
+    assert kda.version() >= 100
+    for code in range(8):
+        assert kda.status_string(code) not in ("", "unknown status")
+    assert kda.status_string(99) == "unknown status"
+
+
+def _call(lib, **over):
+    fake = ctypes.c_void_p(0x10000)  # never dereferenced: validation fails first
+    args = dict(q=fake, k=fake, v=fake, g=fake, beta=fake, cu=fake, N=2, T=100, H=4, dk=128, dv=128,
+                s0=None, scale=0.088, lb=-5.0, o=fake, sT=None, status=None, stream=None)
+    args.update(over)
+    return lib.kda_chunk_fwd(args["q"], args["k"], args["v"], args["g"], args["beta"], args["cu"],
+                             args["N"], args["T"], args["H"], args["dk"], args["dv"], args["s0"],
+                             args["scale"], args["lb"], args["o"], args["sT"], args["status"],
+                             args["stream"])
+
+
+@pytest.mark.parametrize("over,code", [
+    ({"dk": 64}, kda.KDA_ERR_UNSUPPORTED),
+    ({"dv": 256}, kda.KDA_ERR_UNSUPPORTED),
+    ({"H": 0}, kda.KDA_ERR_INVALID_ARG),
+    ({"N": -1}, kda.KDA_ERR_INVALID_ARG),
+    ({"T": -5}, kda.KDA_ERR_INVALID_ARG),
+    ({"lb": -20.0}, kda.KDA_ERR_INVALID_ARG),
+    ({"lb": 0.5}, kda.KDA_ERR_INVALID_ARG),
+    ({"scale": float("nan")}, kda.KDA_ERR_INVALID_ARG),
+    ({"q": None}, kda.KDA_ERR_INVALID_ARG),
+    ({"g": None}, kda.KDA_ERR_INVALID_ARG),
+    ({"cu": None}, kda.KDA_ERR_INVALID_ARG),
+    ({"o": None}, kda.KDA_ERR_INVALID_ARG),
+    ({"q": ctypes.c_void_p(0x10008)}, kda.KDA_ERR_INVALID_ARG),  # not 16-byte aligned
+    ({"s0": ctypes.c_void_p(0x10004)}, kda.KDA_ERR_INVALID_ARG),
+    ({"N": 0, "T": 5}, kda.KDA_ERR_INVALID_ARG),
+])
+def test_host_validation_rejects(lib, over, code):
+    assert _call(lib, **over) == code
+
+
+def test_empty_problem_is_a_no_op(lib):
+    assert _call(lib, N=0, T=0, q=None, k=None, v=None, g=None, beta=None, o=None, cu=None) == kda.KDA_OK
+    assert kda.chunk_fwd_launches(0, 0, 4) == 0
+    assert kda.chunk_fwd_launches(4, 8192, 16) == 1
