@@ -366,7 +366,7 @@ def bench_gpu(a, world, rank, local):
     alg_bytes = algorithmic_bytes(T, N, H, with_init)
     mean_launch_s = (sum(step_ms) / len(step_ms)) / 1e3
     achieved_gbs = alg_bytes / mean_launch_s / 1e9
-    kernel = "kda_chain_mma_kernel"
+    kernel = "kda_persistent_kernel"
     traffic = traffic_from_profile(a.workload, kernel)
     flops = algorithmic_flops(inp["seqlens"], H)
 

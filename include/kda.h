@@ -22,8 +22,10 @@
  *
  * General contract
  *   - Every pointer argument is CUDA device memory owned by the caller
- *     (except where stated). The library allocates nothing per call and keeps
- *     no state between calls; calls are thread-safe.
+ *     (except where stated). The library allocates nothing: scratch space is a
+ *     caller-provided workspace (kda_chunk_fwd_workspace_size). It keeps no
+ *     state between calls; calls are thread-safe as long as concurrent calls
+ *     use different workspaces.
  *   - Calls are asynchronous on `stream`. Argument errors detected on the host
  *     are returned synchronously and nothing is launched. Data errors detected
  *     on the device are written to *status_dev (when given); the outputs are
@@ -33,6 +35,7 @@
 #ifndef KDA_GB300_KDA_H
 #define KDA_GB300_KDA_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -102,6 +105,15 @@ typedef enum {
  *   fp16 operands. The state stays fp32 across the whole sequence. Inputs must
  *   keep |v|, |initial_state| and the state below ~6e4 (fp16 operand range);
  *   otherwise KDA_ERR_VALUE_RANGE is reported.
+ *   workspace     device scratch of at least kda_chunk_fwd_workspace_size(num_seqs,
+ *                 num_heads) bytes, 16-byte aligned, used by one call at a time
+ *                 (its first bytes are reset on the stream at every call; calls
+ *                 that overlap on the GPU must not share it).
+ * Execution: one persistent kernel with one CTA per SM, launched cooperatively
+ *   (all CTAs resident). Producer CTAs run the intra-chunk steps for
+ *   (chain, chunk) tasks and hand the results through a ring in the workspace
+ *   to consumer CTAs that own the chains and carry the state; every wait is
+ *   bounded and a wait that runs out reports KDA_ERR_TIMEOUT.
  * Returns KDA_OK once the work is queued, or a host-side error code with
  * nothing launched. num_seqs == 0 launches nothing.
  */
@@ -110,7 +122,12 @@ kda_status_t kda_chunk_fwd(const void *q, const void *k, const void *v, const fl
                            int64_t total_tokens, int32_t num_heads, int32_t head_dim_k,
                            int32_t head_dim_v, const float *initial_state, float scale,
                            float lower_bound, float *o, float *final_state,
-                           int32_t *status_dev, kda_stream_t stream);
+                           int32_t *status_dev, void *workspace, size_t workspace_bytes,
+                           kda_stream_t stream);
+
+/* Workspace bytes kda_chunk_fwd needs for these sizes on the current device
+ * (0 when num_seqs or num_heads is 0, or no usable device is current). */
+size_t kda_chunk_fwd_workspace_size(int32_t num_seqs, int32_t num_heads);
 
 /* Number of kernel launches one kda_chunk_fwd call makes for these sizes
  * (0 when num_seqs == 0). Host-only, no CUDA call. */

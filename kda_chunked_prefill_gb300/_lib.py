@@ -26,7 +26,8 @@ KDA_ERR_TIMEOUT = 6
 KDA_ERR_VALUE_RANGE = 7
 
 HEAD_DIM = 128
-EXPORTED = ("kda_chunk_fwd", "kda_chunk_fwd_launches", "kda_status_string", "kda_version")
+EXPORTED = ("kda_chunk_fwd", "kda_chunk_fwd_workspace_size", "kda_chunk_fwd_launches",
+            "kda_status_string", "kda_version")
 
 _lock = threading.Lock()
 _lib = None
@@ -56,8 +57,10 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
         lib = ctypes.CDLL(path)
         vp, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
         lib.kda_chunk_fwd.argtypes = [vp, vp, vp, vp, vp, vp, i32, i64, i32, i32, i32, vp, f32, f32,
-                                      vp, vp, vp, vp]
+                                      vp, vp, vp, vp, ctypes.c_size_t, vp]
         lib.kda_chunk_fwd.restype = ctypes.c_int
+        lib.kda_chunk_fwd_workspace_size.argtypes = [i32, i32]
+        lib.kda_chunk_fwd_workspace_size.restype = ctypes.c_size_t
         lib.kda_chunk_fwd_launches.argtypes = [i32, i64, i32]
         lib.kda_chunk_fwd_launches.restype = i32
         lib.kda_status_string.argtypes = [i32]
@@ -74,6 +77,26 @@ def status_string(code: int) -> str:
 
 def version() -> int:
     return int(load_library().kda_version())
+
+
+def workspace_size(num_seqs: int, num_heads: int) -> int:
+    """Workspace bytes ``kda_chunk_fwd`` needs on the current CUDA device."""
+    return int(load_library().kda_chunk_fwd_workspace_size(int(num_seqs), int(num_heads)))
+
+
+_ws_cache = {}
+
+
+def workspace_for(num_seqs: int, num_heads: int, device) -> torch.Tensor:
+    """A cached workspace buffer for calls on ``device``'s current stream.
+    Calls that may overlap on the GPU need buffers of their own."""
+    need = workspace_size(num_seqs, num_heads)
+    key = torch.device(device)
+    buf = _ws_cache.get(key)
+    if buf is None or buf.numel() < need:
+        buf = torch.empty(max(need, 1), dtype=torch.uint8, device=key)
+        _ws_cache[key] = buf
+    return buf
 
 
 def chunk_fwd_launches(num_seqs: int, total_tokens: int, num_heads: int) -> int:
@@ -96,14 +119,16 @@ def _check(t, name, dtype, shape, device):
 
 
 def kda_chunk_fwd(q, k, v, g, beta, cu_seqlens, initial_state, scale: float, lower_bound: float,
-                  o, final_state, status=None, stream=None) -> int:
+                  o, final_state, status=None, stream=None, workspace=None) -> int:
     """Call the C entry point ``kda_chunk_fwd`` with caller-allocated outputs.
 
     q, k, v: bf16 [T,H,128]; o: fp32 [T,H,128]; g: fp32 [T,H,128]; beta: fp32 [T,H];
     cu_seqlens: int32 [N+1]; initial_state / final_state: fp32 [N,H,128,128]
-    or None; status: int32 [1] or None. All on one CUDA device. ``stream`` is a
-    ``torch.cuda.Stream`` (default: the current stream). Raises ``KdaError`` on a
-    host-side error; returns ``KDA_OK`` once the work is queued.
+    or None; status: int32 [1] or None; workspace: uint8 tensor of at least
+    ``workspace_size(N, H)`` bytes (default: a cached per-device buffer). All on
+    one CUDA device. ``stream`` is a ``torch.cuda.Stream`` (default: the current
+    stream). Raises ``KdaError`` on a host-side error; returns ``KDA_OK`` once
+    the work is queued.
     """
     T, H, D = q.shape
     N = cu_seqlens.shape[0] - 1
@@ -125,10 +150,14 @@ def kda_chunk_fwd(q, k, v, g, beta, cu_seqlens, initial_state, scale: float, low
         _check(status, "status", torch.int32, (1,), dev)
     if stream is None:
         stream = torch.cuda.current_stream(dev)
+    if workspace is None:
+        workspace = workspace_for(N, H, dev)
+    if workspace.device != dev or workspace.dtype != torch.uint8 or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous uint8 tensor on the inputs' device")
     rc = load_library().kda_chunk_fwd(
         _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), N, T, H, D, v.shape[2],
         _ptr(initial_state), float(scale), float(lower_bound), _ptr(o), _ptr(final_state),
-        _ptr(status), ctypes.c_void_p(stream.cuda_stream))
+        _ptr(status), _ptr(workspace), workspace.numel(), ctypes.c_void_p(stream.cuda_stream))
     if rc != KDA_OK:
         raise KdaError(rc, "kda_chunk_fwd")
     return rc

@@ -5,14 +5,7 @@
 
 #include "kda.h"
 
-namespace kda {
-namespace chain_mma {
-cudaError_t launch(const void *q, const void *k, const void *v, const float *g, const float *beta,
-                   const int32_t *cu_seqlens, int32_t num_seqs, int64_t total_tokens, int32_t H,
-                   const float *initial_state, float scale, float lower_bound, float *o,
-                   float *final_state, int32_t *status, cudaStream_t stream);
-}
-}  // namespace kda
+#include "kda_persistent.h"
 
 namespace {
 
@@ -33,7 +26,8 @@ kda_status_t kda_chunk_fwd(const void *q, const void *k, const void *v, const fl
                            int64_t total_tokens, int32_t num_heads, int32_t head_dim_k,
                            int32_t head_dim_v, const float *initial_state, float scale,
                            float lower_bound, float *o, float *final_state,
-                           int32_t *status_dev, kda_stream_t stream) {
+                           int32_t *status_dev, void *workspace, size_t workspace_bytes,
+                           kda_stream_t stream) {
     if (head_dim_k != KDA_HEAD_DIM || head_dim_v != KDA_HEAD_DIM) return KDA_ERR_UNSUPPORTED;
     if (num_seqs < 0 || total_tokens < 0 || num_heads < 1) return KDA_ERR_INVALID_ARG;
     if (static_cast<int64_t>(num_seqs) * num_heads > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
@@ -51,14 +45,39 @@ kda_status_t kda_chunk_fwd(const void *q, const void *k, const void *v, const fl
     if ((initial_state && !aligned(initial_state, 16)) || (final_state && !aligned(final_state, 16)) ||
         (status_dev && !aligned(status_dev, 4)))
         return KDA_ERR_INVALID_ARG;
+    if (!workspace || !aligned(workspace, 16)) return KDA_ERR_INVALID_ARG;
+    const size_t need = kda::pers::workspace_bytes(static_cast<int64_t>(num_seqs) * num_heads);
+    if (need == 0) return KDA_ERR_CUDA;
+    if (workspace_bytes < need) return KDA_ERR_INVALID_ARG;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (status_dev && cudaMemsetAsync(status_dev, 0, sizeof(int32_t), s) != cudaSuccess)
         return KDA_ERR_CUDA;
-    const cudaError_t e = kda::chain_mma::launch(q, k, v, g, beta, cu_seqlens, num_seqs, total_tokens,
-                                                 num_heads, initial_state, scale, lower_bound, o,
-                                                 final_state, status_dev, s);
+    kda::pers::Params p;
+    p.q = static_cast<const __nv_bfloat16 *>(q);
+    p.k = static_cast<const __nv_bfloat16 *>(k);
+    p.v = static_cast<const __nv_bfloat16 *>(v);
+    p.g = g;
+    p.beta = beta;
+    p.cu = cu_seqlens;
+    p.N = num_seqs;
+    p.T = total_tokens;
+    p.H = num_heads;
+    p.s0 = initial_state;
+    p.scale = scale;
+    p.lb = lower_bound;
+    p.o = o;
+    p.sT = final_state;
+    p.status = status_dev;
+    p.ws = static_cast<unsigned char *>(workspace);
+    p.C = 0;
+    const cudaError_t e = kda::pers::launch(p, workspace_bytes, s);
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+size_t kda_chunk_fwd_workspace_size(int32_t num_seqs, int32_t num_heads) {
+    if (num_seqs < 1 || num_heads < 1) return 0;
+    return kda::pers::workspace_bytes(static_cast<int64_t>(num_seqs) * num_heads);
 }
 
 int32_t kda_chunk_fwd_launches(int32_t num_seqs, int64_t total_tokens, int32_t num_heads) {

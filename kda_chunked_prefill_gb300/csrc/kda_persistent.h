@@ -1,0 +1,39 @@
+// Internal interface of the persistent producer/consumer kernel (not part of the C ABI).
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace kda {
+namespace pers {
+
+constexpr int RING = 4;              // ring slots per consumer
+constexpr int SLOT_BYTES = 74752;    // one (chain, chunk) hand-off, 1024-byte multiple
+
+struct Params {
+    const __nv_bfloat16 *q, *k, *v;
+    const float *g, *beta;
+    const int32_t *cu;
+    int32_t N;
+    int64_t T;
+    int32_t H;
+    const float *s0;
+    float scale, lb;
+    float *o, *sT;
+    int32_t *status;
+    unsigned char *ws;
+    int32_t C;  // consumer CTAs (set by launch)
+};
+
+// workspace: [64-byte header][ready C*RING][freed C*RING] padded to 1024, then the slots
+__host__ __device__ constexpr size_t ring_offset(int C) {
+    return ((64 + 8 * static_cast<size_t>(C) * RING) + 1023) / 1024 * 1024;
+}
+
+int consumers_for(int64_t chains, int grid);
+size_t workspace_bytes(int64_t chains);
+cudaError_t launch(Params p, size_t ws_bytes, cudaStream_t stream);
+
+}  // namespace pers
+}  // namespace kda

@@ -90,7 +90,7 @@ def test_final_state_in_place_over_initial_state():
     st = d["initial_state"].clone()
     o = torch.empty(d["v"].shape, dtype=torch.float32, device=d["v"].device)
     kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], st, inp["scale"],
-                  inp["lower_bound"], o, st)
+                  inp["lower_bound"], o, st)  # default workspace
     torch.cuda.synchronize()
     assert torch.equal(o, o_ref) and torch.equal(st, f_ref)
 

@@ -51,12 +51,13 @@ def test_version_and_status_strings(lib):
 def _call(lib, **over):
     fake = ctypes.c_void_p(0x10000)  # never dereferenced: validation fails first
     args = dict(q=fake, k=fake, v=fake, g=fake, beta=fake, cu=fake, N=2, T=100, H=4, dk=128, dv=128,
-                s0=None, scale=0.088, lb=-5.0, o=fake, sT=None, status=None, stream=None)
+                s0=None, scale=0.088, lb=-5.0, o=fake, sT=None, status=None, ws=fake, wsb=1 << 20,
+                stream=None)
     args.update(over)
     return lib.kda_chunk_fwd(args["q"], args["k"], args["v"], args["g"], args["beta"], args["cu"],
                              args["N"], args["T"], args["H"], args["dk"], args["dv"], args["s0"],
                              args["scale"], args["lb"], args["o"], args["sT"], args["status"],
-                             args["stream"])
+                             args["ws"], args["wsb"], args["stream"])
 
 
 @pytest.mark.parametrize("over,code", [
@@ -75,9 +76,16 @@ def _call(lib, **over):
     ({"q": ctypes.c_void_p(0x10008)}, kda.KDA_ERR_INVALID_ARG),  # not 16-byte aligned
     ({"s0": ctypes.c_void_p(0x10004)}, kda.KDA_ERR_INVALID_ARG),
     ({"N": 0, "T": 5}, kda.KDA_ERR_INVALID_ARG),
+    ({"ws": None}, kda.KDA_ERR_INVALID_ARG),
+    ({"ws": ctypes.c_void_p(0x10008)}, kda.KDA_ERR_INVALID_ARG),
 ])
 def test_host_validation_rejects(lib, over, code):
     assert _call(lib, **over) == code
+
+
+def test_workspace_size_is_zero_for_empty_problems(lib):
+    assert kda.workspace_size(0, 4) == 0
+    assert kda.workspace_size(3, 0) == 0
 
 
 def test_empty_problem_is_a_no_op(lib):
