@@ -53,8 +53,10 @@ typedef enum {
     KDA_ERR_GATE_RANGE = 4,  /* device: some g outside [lower_bound, 0] or not finite */
     KDA_ERR_BAD_SEQLENS = 5, /* device: cu_seqlens not 0 .. total_tokens nondecreasing */
     KDA_ERR_TIMEOUT = 6,     /* device: a bounded wait inside a kernel gave up */
-    KDA_ERR_VALUE_RANGE = 7  /* device: a value entering an fp16 tensor-core operand
+    KDA_ERR_VALUE_RANGE = 7, /* device: a value entering an fp16 tensor-core operand
                                 exceeded 6e4 in magnitude (or was not finite) */
+    KDA_ERR_SCRATCH_TOO_SMALL = 8 /* kda_chunk_fwd_static_scratch: the problem needs more
+                                     scratch than KDA_STATIC_SCRATCH_BYTES */
 } kda_status_t;
 
 #define KDA_HEAD_DIM 128
@@ -128,6 +130,43 @@ kda_status_t kda_chunk_fwd(const void *q, const void *k, const void *v, const fl
 /* Workspace bytes kda_chunk_fwd needs for these sizes on the current device
  * (0 when num_seqs or num_heads is 0, or no usable device is current). */
 size_t kda_chunk_fwd_workspace_size(int32_t num_seqs, int32_t num_heads);
+
+/* Size of the fixed device scratch array behind kda_chunk_fwd_static_scratch. */
+#define KDA_STATIC_SCRATCH_BYTES (24u << 20)
+
+/*
+ * kda_chunk_fwd_static_scratch — kda_chunk_fwd for callers that cannot allocate
+ * device memory, not even a workspace: for example a runtime whose device
+ * memory is a fixed arena planned before it starts, a real-time host that
+ * forbids allocation after start-up, or a plugin that receives its input and
+ * output tensors but cannot request memory. (The TPU report has no
+ * counterpart: this is a deployment convenience of this library.)
+ *
+ * Arguments, layouts, results and asynchronous behaviour are those of
+ * kda_chunk_fwd, without the workspace pair. The scratch instead comes from
+ * one fixed __device__ array of KDA_STATIC_SCRATCH_BYTES (24 MiB) compiled into
+ * the library, which every GPU that loads the library holds until the process
+ * exits. No call allocates or frees memory.
+ *
+ * The first call made on a device looks up the array's device address with
+ * cudaGetSymbolAddress while that device is current; make that first call
+ * before any stream capture. Every call on a device shares the one array and
+ * it keeps the previous call's contents (the part that must start at zero is
+ * cleared on the stream by each call), so calls whose GPU work may overlap
+ * (different streams, or different host threads) race on it and must be
+ * serialised by the caller.
+ *
+ * Returns KDA_ERR_SCRATCH_TOO_SMALL, with nothing launched, when
+ * kda_chunk_fwd_workspace_size(num_seqs, num_heads) exceeds
+ * KDA_STATIC_SCRATCH_BYTES; otherwise what kda_chunk_fwd returns.
+ */
+kda_status_t kda_chunk_fwd_static_scratch(const void *q, const void *k, const void *v, const float *g,
+                                          const float *beta, const int32_t *cu_seqlens,
+                                          int32_t num_seqs, int64_t total_tokens, int32_t num_heads,
+                                          int32_t head_dim_k, int32_t head_dim_v,
+                                          const float *initial_state, float scale, float lower_bound,
+                                          float *o, float *final_state, int32_t *status_dev,
+                                          kda_stream_t stream);
 
 /* Number of kernel launches one kda_chunk_fwd call makes for these sizes
  * (0 when num_seqs == 0). Host-only, no CUDA call. */

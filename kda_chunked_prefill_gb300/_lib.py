@@ -24,6 +24,7 @@ KDA_ERR_GATE_RANGE = 4
 KDA_ERR_BAD_SEQLENS = 5
 KDA_ERR_TIMEOUT = 6
 KDA_ERR_VALUE_RANGE = 7
+KDA_ERR_SCRATCH_TOO_SMALL = 8
 
 HEAD_DIM = 128
 EXPORTED = ("kda_chunk_fwd", "kda_chunk_fwd_workspace_size", "kda_chunk_fwd_launches",

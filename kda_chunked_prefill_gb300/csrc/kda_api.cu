@@ -95,6 +95,7 @@ const char *kda_status_string(int32_t status) {
         case KDA_ERR_BAD_SEQLENS: return "cu_seqlens not nondecreasing from 0 to total_tokens";
         case KDA_ERR_TIMEOUT: return "a bounded wait inside a kernel gave up";
         case KDA_ERR_VALUE_RANGE: return "a value entering an fp16 tensor-core operand exceeded 6e4 or was not finite";
+        case KDA_ERR_SCRATCH_TOO_SMALL: return "problem needs more scratch than the static scratch array holds";
         default: return "unknown status";
     }
 }
