@@ -27,8 +27,9 @@
 namespace kda {
 namespace pers {
 
-constexpr int NCOMP = 256;            // 8 warps, all computing
+constexpr int NCOMP = 512;            // 16 warps, all computing (<= 128 registers each)
 constexpr int NTHREADS = NCOMP;
+constexpr int NWARPS = NCOMP / 32;
 constexpr long long SPIN_LIMIT = 1ll << 24;
 
 // ---------------------------------------------------------------- slot layout
@@ -64,7 +65,7 @@ __device__ __forceinline__ int at_addr(int lane, int rows, int m0, int k0) {  //
     return tile_chunk(rows, k0 + ((mi >> 1) << 3) + rr, m0 + ((mi & 1) << 3));
 }
 
-__device__ __forceinline__ void sync_compute() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+__device__ __forceinline__ void sync_compute() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
 
 // Optional event trace (compiled in only with -DKDA_TRACE): per CTA, up to
 // TRACE_EVENTS records {globaltimer ns, tag, value} after the ring in the workspace.
@@ -182,9 +183,9 @@ constexpr int RSB = 136, RSF = 136, RSA = 72, RSI = 24;
 constexpr int SZ_T = BT * RSB * 2;        // 17408
 constexpr int SZ_F = BT * RSF * 4;        // 34816
 constexpr int OFF_Q = 0;                  // q -> q*a (bf16 hi)
-constexpr int OFF_QLO = OFF_Q + SZ_T;     // q*a (bf16 lo)
+constexpr int OFF_QLO = OFF_Q + SZ_T;     // q*a (bf16 lo); v / u of the next task (roles swap per task)
 constexpr int OFF_K = OFF_QLO + SZ_T;     // k -> k*a (bf16)
-constexpr int OFF_V = OFF_K + SZ_T;       // v -> beta*v -> u (fp16)
+constexpr int OFF_V = OFF_K + SZ_T;       // v -> beta*v -> u (fp16); q*a lo of the next task
 constexpr int OFF_RK = OFF_V + SZ_T;      // beta*k*e^G -> w (fp16)
 constexpr int OFF_G = OFF_RK + SZ_T;      // g -> G (fp32)
 constexpr int OFF_KB = OFF_G + SZ_F;      // k*e^(G_m - G) (fp32)
@@ -202,13 +203,73 @@ __device__ __forceinline__ int f_pair(int i, int j) { return i * (i - 1) / 2 + j
 __device__ __forceinline__ bool f16_ok(float x) { return fabsf(x) < F16_SAFE; }
 
 // One (chain, chunk) task: steps 1-4, results into the global slot.
+struct Task {
+    int valid, k, j, ch, c;
+};
+
+// next valid task (thread 0): tasks are numbered j * C + k so every consumer advances together
+__device__ __forceinline__ Task fetch_task(const Params &p, const Ring &R, int jmax) {
+    Task t{0, 0, 0, 0, 0};
+    while (true) {
+        const int task = atomicAdd(&R.hdr->counter, 1);
+        t.k = task % p.C;
+        t.j = task / p.C;
+        if (t.j >= jmax) return t;
+        if (map_task(p, t.k, t.j, t.ch, t.c)) {
+            t.valid = 1;
+            return t;
+        }
+    }
+}
+
+// cp.async of part of one task's inputs (rows >= nv zero-filled):
+// part 0: g; part 1: q, k, v (v into vbuf) and beta.
+__device__ __forceinline__ void issue_loads(const Params &p, unsigned char *smem, const Task &tk, int part, int vbuf) {
+    const int tid = threadIdx.x;
+    const int h = tk.ch % p.H;
+    int64_t bos, len;
+    chain_info(p, tk.ch, bos, len);
+    const int64_t t0 = bos + static_cast<int64_t>(tk.c) * BT;
+    const int nv = static_cast<int>((bos + len - t0) < BT ? (bos + len - t0) : BT);
+    const size_t rs = static_cast<size_t>(p.H) * DK;
+    const size_t base = (static_cast<size_t>(t0) * p.H + h) * DK;
+    if (part == 0) {
+        float *sG = reinterpret_cast<float *>(smem + OFF_G);
+        for (int idx = tid; idx < BT * 32; idx += NCOMP) {
+            const int r = idx >> 5, c4 = (idx & 31) << 2;
+            const bool ok = r < nv;
+            cp_async16(sG + r * RSF + c4, p.g + base + (ok ? r * rs : 0) + c4, ok ? 16 : 0);
+        }
+    } else {
+        __nv_bfloat16 *sQ = reinterpret_cast<__nv_bfloat16 *>(smem + OFF_Q);
+        __nv_bfloat16 *sK = reinterpret_cast<__nv_bfloat16 *>(smem + OFF_K);
+        __nv_bfloat16 *sV = reinterpret_cast<__nv_bfloat16 *>(smem + vbuf);
+        for (int idx = tid; idx < BT * 16; idx += NCOMP) {
+            const int r = idx >> 4, c8 = (idx & 15) << 3;
+            const bool ok = r < nv;
+            const size_t off = base + (ok ? r * rs : 0) + c8;
+            cp_async16(sQ + r * RSB + c8, p.q + off, ok ? 16 : 0);
+            cp_async16(sK + r * RSB + c8, p.k + off, ok ? 16 : 0);
+            cp_async16(sV + r * RSB + c8, p.v + off, ok ? 16 : 0);
+        }
+        if (tid < BT) {
+            const bool ok = tid < nv;
+            cp_async4(smem + OFF_BETA + 4 * tid, p.beta + static_cast<size_t>(t0 + (ok ? tid : 0)) * p.H + h, ok ? 4 : 0);
+        }
+    }
+    cp_async_commit();
+}
+
+// One (chain, chunk) task: steps 1-4, results into the global slot. Its inputs
+// were loaded by issue_loads; `vbuf` holds v (then u), `qlobuf` receives q*a lo
+// and then the next task's v. `nxt` (valid or not) is loaded as buffers free up.
 __device__ __forceinline__ void run_task(const Params &p, unsigned char *smem, unsigned char *slot, int ch, int c,
-                                         bool &gate_bad, bool &range_bad) {
+                                         int vbuf, int qlobuf, const Task &nxt, bool &gate_bad, bool &range_bad) {
     __nv_bfloat16 *sQ = reinterpret_cast<__nv_bfloat16 *>(smem + OFF_Q);
-    __nv_bfloat16 *sQlo = reinterpret_cast<__nv_bfloat16 *>(smem + OFF_QLO);
+    __nv_bfloat16 *sQlo = reinterpret_cast<__nv_bfloat16 *>(smem + qlobuf);
     __nv_bfloat16 *sK = reinterpret_cast<__nv_bfloat16 *>(smem + OFF_K);
-    __nv_bfloat16 *sV = reinterpret_cast<__nv_bfloat16 *>(smem + OFF_V);
-    __half *sRV = reinterpret_cast<__half *>(smem + OFF_V);
+    __nv_bfloat16 *sV = reinterpret_cast<__nv_bfloat16 *>(smem + vbuf);
+    __half *sRV = reinterpret_cast<__half *>(smem + vbuf);
     __half *sRK = reinterpret_cast<__half *>(smem + OFF_RK);
     float *sG = reinterpret_cast<float *>(smem + OFF_G);
     float *sKB = reinterpret_cast<float *>(smem + OFF_KB);
@@ -221,89 +282,70 @@ __device__ __forceinline__ void run_task(const Params &p, unsigned char *smem, u
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int gq = lane >> 2, qd = lane & 3;
-    const int H = p.H, h = ch % H;
-    int64_t bos, len;
-    chain_info(p, ch, bos, len);
-    const int64_t t0 = bos + static_cast<int64_t>(c) * BT;
-    const int nv = static_cast<int>((bos + len - t0) < BT ? (bos + len - t0) : BT);
-    const size_t row_stride = static_cast<size_t>(H) * DK;
     const float scale = p.scale;
-
-    // ---- load the chunk (rows >= nv zero-filled)
+    (void)ch;
+    (void)c;
+    // ---- step 1: inclusive prefix sum of g (base 2) per key channel, four
+    // 16-row quarters per channel on all 512 threads, then the per-channel tables
     {
-        const size_t base = (static_cast<size_t>(t0) * H + h) * DK;
-        for (int idx = tid; idx < BT * 16; idx += NCOMP) {
-            const int r = idx >> 4, c8 = (idx & 15) << 3;
-            const bool ok = r < nv;
-            const size_t off = base + (ok ? r * row_stride : 0) + c8;
-            cp_async16(sQ + r * RSB + c8, p.q + off, ok ? 16 : 0);
-            cp_async16(sK + r * RSB + c8, p.k + off, ok ? 16 : 0);
-            cp_async16(sV + r * RSB + c8, p.v + off, ok ? 16 : 0);
-        }
-        for (int idx = tid; idx < BT * 32; idx += NCOMP) {
-            const int r = idx >> 5, c4 = (idx & 31) << 2;
-            const bool ok = r < nv;
-            cp_async16(sG + r * RSF + c4, p.g + base + (ok ? r * row_stride : 0) + c4, ok ? 16 : 0);
-        }
-        if (tid < BT) sBeta[tid] = tid < nv ? p.beta[static_cast<size_t>(t0 + tid) * H + h] : 0.f;
-        cp_async_commit();
-        cp_async_wait_all();
-    }
-    sync_compute();
-    KDA_TRACE_EV(p, 20, 0);
-
-    // ---- step 1: inclusive prefix sum of g (base 2) per key channel + tables
-    if (tid < DK) {
-        const int chn = tid;
+        const int chn = tid & 127, rq = tid >> 7;
+        float x[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) x[q] = sG[(16 * rq + q) * RSF + chn];
         float acc = 0.f;
         bool gb = false;
 #pragma unroll
-        for (int r0 = 0; r0 < BT; r0 += 16) {
-            float x[16];
-#pragma unroll
-            for (int r = 0; r < 16; ++r) x[r] = sG[(r0 + r) * RSF + chn];
-#pragma unroll
-            for (int r = 0; r < 16; ++r) {
-                gb |= !(x[r] >= p.lb && x[r] <= 0.f);
-                acc += x[r] * LOG2E;
-                sG[(r0 + r) * RSF + chn] = acc;
-                if (r == 7) sTab[TGM + (r0 >> 4) * 128 + chn] = acc;
-            }
+        for (int q = 0; q < 16; ++q) {
+            gb |= !(x[q] >= p.lb && x[q] <= 0.f);
+            acc += x[q] * LOG2E;
+            x[q] = acc;
         }
-        const float gl = acc;  // rows >= nv carry g = 0
-        sTab[TGL + chn] = gl;
-        sTab[TD + chn] = ex2(gl);
+        gate_bad |= gb;
+        sTab[TEM + rq * 128 + chn] = acc;  // quarter totals (the EM rows are rebuilt below)
+        sync_compute();
+        float cy = 0.f;
+        for (int q = 0; q < rq; ++q) cy += sTab[TEM + q * 128 + chn];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) sG[(16 * rq + q) * RSF + chn] = x[q] + cy;
+    }
+    sync_compute();
+    if (tid < DK) {  // rows >= nv carry g = 0, so row 63 holds the last valid prefix
+        const int chn = tid;
         float gm[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) gm[i] = sTab[TGM + i * 128 + chn];
+        for (int i = 0; i < 4; ++i) gm[i] = sG[(16 * i + 7) * RSF + chn];
+        const float gl = sG[63 * RSF + chn];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
+            sTab[TGM + i * 128 + chn] = gm[i];
             sTab[TEM + i * 128 + chn] = ex2(gm[i]);
             sTab[TEL + i * 128 + chn] = ex2(gl - gm[i]);
         }
+        sTab[TGL + chn] = gl;
+        sTab[TD + chn] = ex2(gl);
 #pragma unroll
         for (int i = 1; i < 4; ++i)
 #pragma unroll
             for (int j = 0; j < i; ++j) sTab[TF + f_pair(i, j) * 128 + chn] = ex2(gm[i] - gm[j]);
-        gate_bad |= gb;
     }
     sync_compute();
     KDA_TRACE_EV(p, 21, 0);
 
     // ---- steps 2a/4a: elementwise operands; q_hat and kg go straight to the slot
     {
-        float Gv[4][8];
+        float Gv[2][8];
 #pragma unroll
-        for (int it = 0; it < 4; ++it) {
+        for (int it = 0; it < 2; ++it) {
             const int grp = tid + it * NCOMP, r = grp >> 4, c8 = (grp & 15) << 3;
             const float4 a = *reinterpret_cast<const float4 *>(sG + r * RSF + c8);
             const float4 b = *reinterpret_cast<const float4 *>(sG + r * RSF + c8 + 4);
             Gv[it][0] = a.x; Gv[it][1] = a.y; Gv[it][2] = a.z; Gv[it][3] = a.w;
             Gv[it][4] = b.x; Gv[it][5] = b.y; Gv[it][6] = b.z; Gv[it][7] = b.w;
         }
-        sync_compute();  // the gate tile is overwritten below
+        sync_compute();  // the gate tile is free from here on: stream in the next task's g
+        if (nxt.valid) issue_loads(p, smem, nxt, 0, 0);
 #pragma unroll
-        for (int it = 0; it < 4; ++it) {
+        for (int it = 0; it < 2; ++it) {
             const int grp = tid + it * NCOMP, r = grp >> 4, c8 = (grp & 15) << 3;
             const int i = r >> 4;
             const float bt = sBeta[r];
@@ -313,6 +355,18 @@ __device__ __forceinline__ void run_task(const Params &p, unsigned char *smem, u
             const uint32_t *qw = reinterpret_cast<const uint32_t *>(&qv);
             const uint32_t *kw = reinterpret_cast<const uint32_t *>(&kv);
             const uint32_t *vw = reinterpret_cast<const uint32_t *>(&vv);
+            float GM[8], EM[8], EL[8];
+            {
+                const float4 a0 = *reinterpret_cast<const float4 *>(sTab + TGM + i * 128 + c8);
+                const float4 a1 = *reinterpret_cast<const float4 *>(sTab + TGM + i * 128 + c8 + 4);
+                const float4 b0 = *reinterpret_cast<const float4 *>(sTab + TEM + i * 128 + c8);
+                const float4 b1 = *reinterpret_cast<const float4 *>(sTab + TEM + i * 128 + c8 + 4);
+                const float4 d0 = *reinterpret_cast<const float4 *>(sTab + TEL + i * 128 + c8);
+                const float4 d1 = *reinterpret_cast<const float4 *>(sTab + TEL + i * 128 + c8 + 4);
+                GM[0] = a0.x; GM[1] = a0.y; GM[2] = a0.z; GM[3] = a0.w; GM[4] = a1.x; GM[5] = a1.y; GM[6] = a1.z; GM[7] = a1.w;
+                EM[0] = b0.x; EM[1] = b0.y; EM[2] = b0.z; EM[3] = b0.w; EM[4] = b1.x; EM[5] = b1.y; EM[6] = b1.z; EM[7] = b1.w;
+                EL[0] = d0.x; EL[1] = d0.y; EL[2] = d0.z; EL[3] = d0.w; EL[4] = d1.x; EL[5] = d1.y; EL[6] = d1.z; EL[7] = d1.w;
+            }
             uint32_t oQh[4], oQl[4], oKa[4], oBv[4], oBk[4], oQs[4], oKg[4];
             float kb[8];
 #pragma unroll
@@ -321,18 +375,18 @@ __device__ __forceinline__ void run_task(const Params &p, unsigned char *smem, u
                 float res[2][6];
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
-                    const int chn = c8 + 2 * q2 + e;
+                    const int ce = 2 * q2 + e;
                     const float qq = e ? qf.y : qf.x, kk = e ? kf.y : kf.x, vv2 = e ? vf.y : vf.x;
-                    const float x = Gv[it][2 * q2 + e] - sTab[TGM + i * 128 + chn];
+                    const float x = Gv[it][ce] - GM[ce];
                     const float a = ex2(x), b = ex2(-x);
-                    const float eG = a * sTab[TEM + i * 128 + chn];
-                    res[e][0] = qq * a;                              // q e^(G - G_m)
-                    res[e][1] = kk * a;                              // k e^(G - G_m)
-                    res[e][2] = bt * vv2;                            // beta v
-                    res[e][3] = bt * kk * eG;                        // beta k e^G
-                    res[e][4] = scale * qq * eG;                     // scale q e^G
-                    res[e][5] = kk * b * sTab[TEL + i * 128 + chn];  // k e^(G_last - G)
-                    kb[2 * q2 + e] = kk * b;                         // k e^(G_m - G)
+                    const float eG = a * EM[ce];
+                    res[e][0] = qq * a;            // q e^(G - G_m)
+                    res[e][1] = kk * a;            // k e^(G - G_m)
+                    res[e][2] = bt * vv2;          // beta v
+                    res[e][3] = bt * kk * eG;      // beta k e^G
+                    res[e][4] = scale * qq * eG;   // scale q e^G
+                    res[e][5] = kk * b * EL[ce];   // k e^(G_last - G)
+                    kb[ce] = kk * b;               // k e^(G_m - G)
                 }
                 split_bf16(res[0][0], res[1][0], oQh[q2], oQl[q2]);
                 oKa[q2] = pack_bf16(res[0][1], res[1][1]);
@@ -359,14 +413,14 @@ __device__ __forceinline__ void run_task(const Params &p, unsigned char *smem, u
     // ---- step 2b: Aqk (split bf16, three products) and Akk (bf16) on the 10
     // lower 16x16 tiles. Tile (i,j) needs k_s e^(G_{m_i} - G_s) for s in
     // sub-block j: the stored k e^(G_{m_j} - G) times e^(G_{m_i} - G_{m_j}) (<= 1).
-    for (int pair = warp; pair < 10; pair += 8) {
+    for (int unit = warp; unit < 20; unit += NWARPS) {
+        const int pair = unit >> 1, nt = unit & 1;
         int i = 0;
         while ((i + 1) * (i + 2) / 2 <= pair) ++i;
         const int j = pair - i * (i + 1) / 2;
-        const float *kbrow0 = sKB + (16 * j + gq) * RSF;
-        const float *kbrow1 = sKB + (16 * j + 8 + gq) * RSF;
+        const float *kbrow = sKB + (16 * j + 8 * nt + gq) * RSF;  // column s = 16j + 8nt + gq
         const float *fr = sTab + TF + (i > j ? f_pair(i, j) : 0) * 128;
-        float aq[2][4] = {}, ak[2][4] = {};
+        float aq[4] = {}, ak[4] = {};
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
             uint32_t fa[4], fl[4], fk[4];
@@ -379,42 +433,33 @@ __device__ __forceinline__ void run_task(const Params &p, unsigned char *smem, u
                 f0 = *reinterpret_cast<const float2 *>(fr + c0);
                 f1 = *reinterpret_cast<const float2 *>(fr + c0 + 8);
             }
-            uint32_t bh[2][2], bl[2][2];
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                const float *row = nt ? kbrow1 : kbrow0;
-                const float2 x0 = *reinterpret_cast<const float2 *>(row + c0);
-                const float2 x1 = *reinterpret_cast<const float2 *>(row + c0 + 8);
-                split_bf16(x0.x * f0.x, x0.y * f0.y, bh[nt][0], bl[nt][0]);
-                split_bf16(x1.x * f1.x, x1.y * f1.y, bh[nt][1], bl[nt][1]);
-            }
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                mma16816(aq[nt], fa, bh[nt][0], bh[nt][1]);
-                mma16816(aq[nt], fl, bh[nt][0], bh[nt][1]);
-                mma16816(aq[nt], fa, bl[nt][0], bl[nt][1]);
-                mma16816(ak[nt], fk, bh[nt][0], bh[nt][1]);
-            }
+            const float2 x0 = *reinterpret_cast<const float2 *>(kbrow + c0);
+            const float2 x1 = *reinterpret_cast<const float2 *>(kbrow + c0 + 8);
+            uint32_t bh0, bl0, bh1, bl1;
+            split_bf16(x0.x * f0.x, x0.y * f0.y, bh0, bl0);
+            split_bf16(x1.x * f1.x, x1.y * f1.y, bh1, bl1);
+            mma16816(aq, fa, bh0, bh1);
+            mma16816(aq, fl, bh0, bh1);
+            mma16816(aq, fa, bl0, bl1);
+            mma16816(ak, fk, bh0, bh1);
         }
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
+        for (int hf = 0; hf < 2; ++hf) {
+            const int tl = gq + 8 * hf, sl = 8 * nt + 2 * qd;
+            const int t = 16 * i + tl, s = 16 * j + sl;
+            const float bt = sBeta[t];
+            float vq[2], vk[2];
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                const int tl = gq + 8 * hf, sl = 8 * nt + 2 * qd;
-                const int t = 16 * i + tl, s = 16 * j + sl;
-                const float bt = sBeta[t];
-                float vq[2], vk[2];
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const bool incl = (i > j) || (sl + e <= tl);
-                    const bool strict = (i > j) || (sl + e < tl);
-                    vq[e] = incl ? scale * aq[nt][2 * hf + e] : 0.f;
-                    vk[e] = strict ? bt * ak[nt][2 * hf + e] : 0.f;
-                    if (i == j) sLD[(i * 16 + tl) * 17 + sl + e] = vk[e];
-                }
-                *reinterpret_cast<uint32_t *>(sAqk + t * RSA + s) = pack_f16(vq[0], vq[1]);
-                *reinterpret_cast<uint32_t *>(sL + t * RSA + s) = pack_f16(vk[0], vk[1]);
+            for (int e = 0; e < 2; ++e) {
+                const bool incl = (i > j) || (sl + e <= tl);
+                const bool strict = (i > j) || (sl + e < tl);
+                vq[e] = incl ? scale * aq[2 * hf + e] : 0.f;
+                vk[e] = strict ? bt * ak[2 * hf + e] : 0.f;
+                if (i == j) sLD[(i * 16 + tl) * 17 + sl + e] = vk[e];
             }
+            *reinterpret_cast<uint32_t *>(sAqk + t * RSA + s) = pack_f16(vq[0], vq[1]);
+            *reinterpret_cast<uint32_t *>(sL + t * RSA + s) = pack_f16(vk[0], vk[1]);
+        }
     }
     // upper tiles of scale*Aqk are zero (the consumer reads the full 64x64)
     for (int idx = tid; idx < 6 * 16 * 8; idx += NCOMP) {
@@ -424,6 +469,8 @@ __device__ __forceinline__ void run_task(const Params &p, unsigned char *smem, u
         *reinterpret_cast<uint32_t *>(sAqk + (16 * i + rr) * RSA + 16 * j + cc) = 0u;
     }
     sync_compute();
+    // q, k, q*a lo, kb and beta are free: stream in the rest of the next task
+    if (nxt.valid) issue_loads(p, smem, nxt, 1, qlobuf);
     KDA_TRACE_EV(p, 23, 0);
 
     // ---- step 3a: (I + L_ii)^-1 for the four diagonal blocks, fp32 substitution
@@ -444,25 +491,21 @@ __device__ __forceinline__ void run_task(const Params &p, unsigned char *smem, u
     sync_compute();
     KDA_TRACE_EV(p, 24, 0);
 
-    // ---- steps 3b/4: X = (I+L)^-1 [beta v | beta k e^G], in place; warp w owns 32 columns
+    // ---- steps 3b/4: X = (I+L)^-1 [beta v | beta k e^G], in place; warp w owns 16 columns
     {
-        __half *R = (warp < 4) ? sRV : sRK;
-        const int col0 = 32 * (warp & 3);
+        __half *R = (warp < 8) ? sRV : sRK;
+        const int col0 = 16 * (warp & 7);
         for (int i = 0; i < 4; ++i) {
-            float acc[4][4] = {};
+            float acc[2][4] = {};
             for (int j = 0; j < i; ++j) {
-                uint32_t fa[4];
+                uint32_t fa[4], fb[4];
                 ldsm_x4(fa, sL + (16 * i + (lane & 15)) * RSA + 16 * j + ((lane >> 4) << 3));
-#pragma unroll
-                for (int nb = 0; nb < 2; ++nb) {
-                    uint32_t fb[4];
-                    ldsm_x4_t(fb, R + bk_off(lane, 16 * j, col0 + 16 * nb, RSB));
-                    mma16816_f16(acc[2 * nb], fa, fb[0], fb[1]);
-                    mma16816_f16(acc[2 * nb + 1], fa, fb[2], fb[3]);
-                }
+                ldsm_x4_t(fb, R + bk_off(lane, 16 * j, col0, RSB));
+                mma16816_f16(acc[0], fa, fb[0], fb[1]);
+                mma16816_f16(acc[1], fa, fb[2], fb[3]);
             }
 #pragma unroll
-            for (int nt = 0; nt < 4; ++nt)
+            for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
                     uint32_t *pp = reinterpret_cast<uint32_t *>(R + (16 * i + gq + 8 * hf) * RSB + col0 + 8 * nt + 2 * qd);
@@ -472,21 +515,17 @@ __device__ __forceinline__ void run_task(const Params &p, unsigned char *smem, u
                     *pp = pack_f16(y0, y1);
                 }
             __syncwarp();
-            float xo[4][4] = {};
+            float xo[2][4] = {};
             {
-                uint32_t fa[4];
+                uint32_t fa[4], fb[4];
                 ldsm_x4(fa, sInv + (16 * i + (lane & 15)) * RSI + ((lane >> 4) << 3));
-#pragma unroll
-                for (int nb = 0; nb < 2; ++nb) {
-                    uint32_t fb[4];
-                    ldsm_x4_t(fb, R + bk_off(lane, 16 * i, col0 + 16 * nb, RSB));
-                    mma16816_f16(xo[2 * nb], fa, fb[0], fb[1]);
-                    mma16816_f16(xo[2 * nb + 1], fa, fb[2], fb[3]);
-                }
+                ldsm_x4_t(fb, R + bk_off(lane, 16 * i, col0, RSB));
+                mma16816_f16(xo[0], fa, fb[0], fb[1]);
+                mma16816_f16(xo[1], fa, fb[2], fb[3]);
             }
             __syncwarp();
 #pragma unroll
-            for (int nt = 0; nt < 4; ++nt)
+            for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
                     const int rr = 16 * i + gq + 8 * hf, cc = col0 + 8 * nt + 2 * qd;
@@ -530,28 +569,47 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int pi
     }
     sync_compute();
     const int jmax = misc[1];
-    bool gate_bad = false, range_bad = false;
-    while (true) {
-        if (tid == 0) misc[0] = atomicAdd(&R.hdr->counter, 1);
+    auto fetch = [&]() {  // all threads; thread 0 draws, everyone reads after the barrier
+        if (tid == 0) {
+            const Task t = fetch_task(p, R, jmax);
+            misc[2] = t.valid; misc[3] = t.k; misc[4] = t.j; misc[5] = t.ch; misc[6] = t.c;
+        }
         sync_compute();
-        const int task = misc[0];
-        const int k = task % p.C, j = task / p.C;
-        sync_compute();  // misc[0] read before it is rewritten
-        if (j >= jmax) break;
-        int ch, c;
-        if (!map_task(p, k, j, ch, c)) continue;
-        const int s = j % RING;
-        KDA_TRACE_EV(p, 1, task);
-        if (tid == 0) misc[2] = (j < RING) ? 1 : (wait_flag_geq(R, &R.freed[k * RING + s], j - RING + 1, p.status) ? 1 : 0);
+        const Task t{misc[2], misc[3], misc[4], misc[5], misc[6]};
         sync_compute();
-        if (!misc[2]) break;
-        unsigned char *slot = R.slots + static_cast<size_t>(k * RING + s) * SLOT_BYTES;
-        run_task(p, smem, slot, ch, c, gate_bad, range_bad);
-        __threadfence();
-        sync_compute();
-        if (tid == 0) st_release(&R.ready[k * RING + s], j + 1);
-        KDA_TRACE_EV(p, 3, task);
+        return t;
+    };
+    Task cur = fetch();
+    int vbuf = OFF_V, qlobuf = OFF_QLO;
+    if (cur.valid) {
+        issue_loads(p, smem, cur, 0, vbuf);
+        issue_loads(p, smem, cur, 1, vbuf);
     }
+    bool gate_bad = false, range_bad = false;
+    while (cur.valid) {
+        const Task nxt = fetch();
+        const int s = cur.j % RING;
+        KDA_TRACE_EV(p, 1, cur.j * p.C + cur.k);
+        if (tid == 0)
+            misc[7] = (cur.j < RING) ? 1 : (wait_flag_geq(R, &R.freed[cur.k * RING + s], cur.j - RING + 1, p.status) ? 1 : 0);
+        cp_async_wait_all();
+        sync_compute();
+        if (!misc[7]) break;
+        KDA_TRACE_EV(p, 20, 0);
+        unsigned char *slot = R.slots + static_cast<size_t>(cur.k * RING + s) * SLOT_BYTES;
+        run_task(p, smem, slot, cur.ch, cur.c, vbuf, qlobuf, nxt, gate_bad, range_bad);
+        sync_compute();
+        if (tid == 0) {
+            __threadfence();
+            st_release(&R.ready[cur.k * RING + s], cur.j + 1);
+        }
+        KDA_TRACE_EV(p, 3, cur.j * p.C + cur.k);
+        cur = nxt;
+        const int tmp = vbuf;
+        vbuf = qlobuf;
+        qlobuf = tmp;
+    }
+    cp_async_wait_all();
     if (gate_bad) set_status(p.status, KDA_ERR_GATE_RANGE);
     if (range_bad) set_status(p.status, KDA_ERR_VALUE_RANGE);
 }
@@ -561,8 +619,8 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int pi
 // Step 5 on the 5th-generation tensor cores. TMEM holds the fp32 state S
 // (columns 0-127, lane = key channel) and the accumulator D = [q_hat S ; w S]
 // (columns 128-255, lanes 0-63 = tokens of q_hat S, lanes 64-127 = tokens of
-// w S). One thread issues the MMAs; all eight warps run the epilogues, warp w
-// on TMEM lanes 32*(w%4).. and value columns 64*(w/4)..
+// w S). One thread issues the MMAs; all sixteen warps run the epilogues, warp w
+// on TMEM lanes 32*(w%4).. and value columns 32*(w/4)..
 //   MMA1  D  = [q_hat ; w] (K-major, 128 x 128) * S16 (fp16 snapshot, MN-major)
 //   MMA2  D += [scale*Aqk ; 0] (K-major, 128 x 64) * v_new (MN-major)   (lanes 0-63: o)
 //   MMA3  S += kg^T (MN-major, 128 x 64) * v_new, after S <- Diag(d) S in TMEM
@@ -593,7 +651,7 @@ __device__ __forceinline__ bool wait_all(const Ring &R, uint64_t *bar, uint32_t 
 
 __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int quad = warp & 3, half = warp >> 2;  // TMEM lane quarter, value-column half
+    const int quad = warp & 3, slice = warp >> 2;  // TMEM lane quarter, 32-column value slice
     const int row = 32 * quad + lane;             // this thread's TMEM lane
     Ring R = ring_of(p);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
@@ -620,7 +678,7 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
     sync_compute();
     tc_fence_after();
     const uint32_t tmem = *tslot;
-    const uint32_t tS = tmem + (static_cast<uint32_t>(32 * quad) << 16) + 64 * half;  // this thread's S columns
+    const uint32_t tS = tmem + (static_cast<uint32_t>(32 * quad) << 16) + 32 * slice;  // this thread's S columns
     const uint32_t tD = tS + 128;                                                       // this thread's D columns
     const int total = consumer_total(p, k);
 
@@ -655,12 +713,12 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
         }
         const int n = ch / p.H, h = ch % p.H;
         const size_t state_base = (static_cast<size_t>(n) * p.H + h) * (DK * DV);
-        // initial state (or zeros) -> TMEM: row `row`, columns 64*half..+63
+        // initial state (or zeros) -> TMEM: row `row`, columns 32*slice..+31
 #pragma unroll
-        for (int cb = 0; cb < 4; ++cb) {
+        for (int cb = 0; cb < 2; ++cb) {
             uint32_t r[16];
             if (p.s0) {
-                const float4 *src = reinterpret_cast<const float4 *>(p.s0 + state_base + row * DV + 64 * half + 16 * cb);
+                const float4 *src = reinterpret_cast<const float4 *>(p.s0 + state_base + row * DV + 32 * slice + 16 * cb);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const float4 f = src[e];
@@ -710,11 +768,9 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
             // (2) fp16 snapshot of the entry state for MMA1, then S <- Diag(d) S in TMEM
             {
                 const float d = reinterpret_cast<const float *>(bb + SL_D)[row];
-                uint32_t r0[16], r1[16], r2[16], r3[16];
+                uint32_t r0[16], r1[16];
                 tmem_ld16(tS, r0);
                 tmem_ld16(tS + 16, r1);
-                tmem_ld16(tS + 32, r2);
-                tmem_ld16(tS + 48, r3);
                 tmem_wait_ld();
                 auto snap = [&](uint32_t (&r)[16], int cb) {
                     uint32_t hp[8];
@@ -724,7 +780,7 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
                         range_bad |= !(f16_ok(x0) && f16_ok(x1));
                         hp[e] = pack_f16(x0, x1);
                     }
-                    const int c8 = 64 * half + 16 * cb;
+                    const int c8 = 32 * slice + 16 * cb;
                     *reinterpret_cast<uint4 *>(sS + tile_chunk(128, row, c8)) = make_uint4(hp[0], hp[1], hp[2], hp[3]);
                     *reinterpret_cast<uint4 *>(sS + tile_chunk(128, row, c8 + 8)) = make_uint4(hp[4], hp[5], hp[6], hp[7]);
 #pragma unroll
@@ -732,12 +788,8 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
                 };
                 snap(r0, 0);
                 snap(r1, 1);
-                snap(r2, 2);
-                snap(r3, 3);
                 tmem_st16(tS, r0);
                 tmem_st16(tS + 16, r1);
-                tmem_st16(tS + 32, r2);
-                tmem_st16(tS + 48, r3);
                 tmem_wait_st();
             }
             fence_proxy_async_shared();
@@ -762,14 +814,12 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
             KDA_TRACE_EV(p, 14, j);
             if (quad >= 2) {
                 const int t = row - 64;
-                uint32_t r0[16], r1[16], r2[16], r3[16];
+                uint32_t r0[16], r1[16];
                 tmem_ld16(tD, r0);
                 tmem_ld16(tD + 16, r1);
-                tmem_ld16(tD + 32, r2);
-                tmem_ld16(tD + 48, r3);
                 tmem_wait_ld();
                 auto vnew = [&](const uint32_t (&r)[16], int cb) {
-                    const int c8 = 64 * half + 16 * cb;
+                    const int c8 = 32 * slice + 16 * cb;
 #pragma unroll
                     for (int hh = 0; hh < 2; ++hh) {
                         const uint4 uu = *reinterpret_cast<const uint4 *>(bb + SL_U + tile_chunk(64, t, c8 + 8 * hh));
@@ -788,8 +838,6 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
                 };
                 vnew(r0, 0);
                 vnew(r1, 1);
-                vnew(r2, 2);
-                vnew(r3, 3);
             }
             fence_proxy_async_shared();
             tc_fence_before();
@@ -818,23 +866,17 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
             KDA_TRACE_EV(p, 16, j);
             float *stg = reinterpret_cast<float *>(sS);  // [64][OST] fp32, spans the S16 and v_new tiles
             if (quad < 2) {
-                uint32_t r0[16], r1[16], r2[16], r3[16];
+                uint32_t r0[16], r1[16];
                 tmem_ld16(tD, r0);
                 tmem_ld16(tD + 16, r1);
-                tmem_ld16(tD + 32, r2);
-                tmem_ld16(tD + 48, r3);
                 tmem_wait_ld();
-                float *dst = stg + row * OST + 64 * half;
+                float *dst = stg + row * OST + 32 * slice;
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     reinterpret_cast<float4 *>(dst)[e] = make_float4(__uint_as_float(r0[4 * e]), __uint_as_float(r0[4 * e + 1]),
                                                                      __uint_as_float(r0[4 * e + 2]), __uint_as_float(r0[4 * e + 3]));
                     reinterpret_cast<float4 *>(dst + 16)[e] = make_float4(__uint_as_float(r1[4 * e]), __uint_as_float(r1[4 * e + 1]),
                                                                           __uint_as_float(r1[4 * e + 2]), __uint_as_float(r1[4 * e + 3]));
-                    reinterpret_cast<float4 *>(dst + 32)[e] = make_float4(__uint_as_float(r2[4 * e]), __uint_as_float(r2[4 * e + 1]),
-                                                                          __uint_as_float(r2[4 * e + 2]), __uint_as_float(r2[4 * e + 3]));
-                    reinterpret_cast<float4 *>(dst + 48)[e] = make_float4(__uint_as_float(r3[4 * e]), __uint_as_float(r3[4 * e + 1]),
-                                                                          __uint_as_float(r3[4 * e + 2]), __uint_as_float(r3[4 * e + 3]));
                 }
             }
             tc_fence_before();
@@ -855,11 +897,11 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
         if (p.sT) {
             tc_fence_after();
 #pragma unroll
-            for (int cb = 0; cb < 4; ++cb) {
+            for (int cb = 0; cb < 2; ++cb) {
                 uint32_t r[16];
                 tmem_ld16(tS + 16 * cb, r);
                 tmem_wait_ld();
-                float4 *dst = reinterpret_cast<float4 *>(p.sT + state_base + row * DV + 64 * half + 16 * cb);
+                float4 *dst = reinterpret_cast<float4 *>(p.sT + state_base + row * DV + 32 * slice + 16 * cb);
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
                     dst[e] = make_float4(__uint_as_float(r[4 * e]), __uint_as_float(r[4 * e + 1]),
