@@ -333,10 +333,12 @@ __device__ __forceinline__ void run_task(const Params &p, unsigned char *smem, u
 
     // ---- steps 2a/4a: elementwise operands; q_hat and kg go straight to the slot
     {
+        // thread: channels c8..c8+7 of rows r0 and r0 + 8, both in sub-block i
+        const int ew_i = tid >> 7, ew_c8 = (tid & 15) << 3, ew_r0 = 16 * ew_i + ((tid >> 4) & 7);
         float Gv[2][8];
 #pragma unroll
         for (int it = 0; it < 2; ++it) {
-            const int grp = tid + it * NCOMP, r = grp >> 4, c8 = (grp & 15) << 3;
+            const int r = ew_r0 + 8 * it, c8 = ew_c8;
             const float4 a = *reinterpret_cast<const float4 *>(sG + r * RSF + c8);
             const float4 b = *reinterpret_cast<const float4 *>(sG + r * RSF + c8 + 4);
             Gv[it][0] = a.x; Gv[it][1] = a.y; Gv[it][2] = a.z; Gv[it][3] = a.w;
@@ -344,10 +346,22 @@ __device__ __forceinline__ void run_task(const Params &p, unsigned char *smem, u
         }
         sync_compute();  // the gate tile is free from here on: stream in the next task's g
         if (nxt.valid) issue_loads(p, smem, nxt, 0, 0);
+        float GM[8], EM[8], EL[8];
+        {
+            const int i = ew_i, c8 = ew_c8;
+            const float4 a0 = *reinterpret_cast<const float4 *>(sTab + TGM + i * 128 + c8);
+            const float4 a1 = *reinterpret_cast<const float4 *>(sTab + TGM + i * 128 + c8 + 4);
+            const float4 b0 = *reinterpret_cast<const float4 *>(sTab + TEM + i * 128 + c8);
+            const float4 b1 = *reinterpret_cast<const float4 *>(sTab + TEM + i * 128 + c8 + 4);
+            const float4 d0 = *reinterpret_cast<const float4 *>(sTab + TEL + i * 128 + c8);
+            const float4 d1 = *reinterpret_cast<const float4 *>(sTab + TEL + i * 128 + c8 + 4);
+            GM[0] = a0.x; GM[1] = a0.y; GM[2] = a0.z; GM[3] = a0.w; GM[4] = a1.x; GM[5] = a1.y; GM[6] = a1.z; GM[7] = a1.w;
+            EM[0] = b0.x; EM[1] = b0.y; EM[2] = b0.z; EM[3] = b0.w; EM[4] = b1.x; EM[5] = b1.y; EM[6] = b1.z; EM[7] = b1.w;
+            EL[0] = d0.x; EL[1] = d0.y; EL[2] = d0.z; EL[3] = d0.w; EL[4] = d1.x; EL[5] = d1.y; EL[6] = d1.z; EL[7] = d1.w;
+        }
 #pragma unroll
         for (int it = 0; it < 2; ++it) {
-            const int grp = tid + it * NCOMP, r = grp >> 4, c8 = (grp & 15) << 3;
-            const int i = r >> 4;
+            const int r = ew_r0 + 8 * it, c8 = ew_c8;
             const float bt = sBeta[r];
             const uint4 qv = *reinterpret_cast<const uint4 *>(sQ + r * RSB + c8);
             const uint4 kv = *reinterpret_cast<const uint4 *>(sK + r * RSB + c8);
@@ -355,18 +369,6 @@ __device__ __forceinline__ void run_task(const Params &p, unsigned char *smem, u
             const uint32_t *qw = reinterpret_cast<const uint32_t *>(&qv);
             const uint32_t *kw = reinterpret_cast<const uint32_t *>(&kv);
             const uint32_t *vw = reinterpret_cast<const uint32_t *>(&vv);
-            float GM[8], EM[8], EL[8];
-            {
-                const float4 a0 = *reinterpret_cast<const float4 *>(sTab + TGM + i * 128 + c8);
-                const float4 a1 = *reinterpret_cast<const float4 *>(sTab + TGM + i * 128 + c8 + 4);
-                const float4 b0 = *reinterpret_cast<const float4 *>(sTab + TEM + i * 128 + c8);
-                const float4 b1 = *reinterpret_cast<const float4 *>(sTab + TEM + i * 128 + c8 + 4);
-                const float4 d0 = *reinterpret_cast<const float4 *>(sTab + TEL + i * 128 + c8);
-                const float4 d1 = *reinterpret_cast<const float4 *>(sTab + TEL + i * 128 + c8 + 4);
-                GM[0] = a0.x; GM[1] = a0.y; GM[2] = a0.z; GM[3] = a0.w; GM[4] = a1.x; GM[5] = a1.y; GM[6] = a1.z; GM[7] = a1.w;
-                EM[0] = b0.x; EM[1] = b0.y; EM[2] = b0.z; EM[3] = b0.w; EM[4] = b1.x; EM[5] = b1.y; EM[6] = b1.z; EM[7] = b1.w;
-                EL[0] = d0.x; EL[1] = d0.y; EL[2] = d0.z; EL[3] = d0.w; EL[4] = d1.x; EL[5] = d1.y; EL[6] = d1.z; EL[7] = d1.w;
-            }
             uint32_t oQh[4], oQl[4], oKa[4], oBv[4], oBk[4], oQs[4], oKg[4];
             float kb[8];
 #pragma unroll
@@ -413,14 +415,14 @@ __device__ __forceinline__ void run_task(const Params &p, unsigned char *smem, u
     // ---- step 2b: Aqk (split bf16, three products) and Akk (bf16) on the 10
     // lower 16x16 tiles. Tile (i,j) needs k_s e^(G_{m_i} - G_s) for s in
     // sub-block j: the stored k e^(G_{m_j} - G) times e^(G_{m_i} - G_{m_j}) (<= 1).
-    for (int unit = warp; unit < 20; unit += NWARPS) {
-        const int pair = unit >> 1, nt = unit & 1;
+    for (int pair = warp; pair < 10; pair += NWARPS) {
         int i = 0;
         while ((i + 1) * (i + 2) / 2 <= pair) ++i;
         const int j = pair - i * (i + 1) / 2;
-        const float *kbrow = sKB + (16 * j + 8 * nt + gq) * RSF;  // column s = 16j + 8nt + gq
+        const float *kbrow0 = sKB + (16 * j + gq) * RSF;      // column s = 16j + gq
+        const float *kbrow1 = sKB + (16 * j + 8 + gq) * RSF;  // column s = 16j + 8 + gq
         const float *fr = sTab + TF + (i > j ? f_pair(i, j) : 0) * 128;
-        float aq[4] = {}, ak[4] = {};
+        float aq[2][4] = {}, ak[2][4] = {};
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
             uint32_t fa[4], fl[4], fk[4];
@@ -433,33 +435,39 @@ __device__ __forceinline__ void run_task(const Params &p, unsigned char *smem, u
                 f0 = *reinterpret_cast<const float2 *>(fr + c0);
                 f1 = *reinterpret_cast<const float2 *>(fr + c0 + 8);
             }
-            const float2 x0 = *reinterpret_cast<const float2 *>(kbrow + c0);
-            const float2 x1 = *reinterpret_cast<const float2 *>(kbrow + c0 + 8);
-            uint32_t bh0, bl0, bh1, bl1;
-            split_bf16(x0.x * f0.x, x0.y * f0.y, bh0, bl0);
-            split_bf16(x1.x * f1.x, x1.y * f1.y, bh1, bl1);
-            mma16816(aq, fa, bh0, bh1);
-            mma16816(aq, fl, bh0, bh1);
-            mma16816(aq, fa, bl0, bl1);
-            mma16816(ak, fk, bh0, bh1);
-        }
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-            const int tl = gq + 8 * hf, sl = 8 * nt + 2 * qd;
-            const int t = 16 * i + tl, s = 16 * j + sl;
-            const float bt = sBeta[t];
-            float vq[2], vk[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const bool incl = (i > j) || (sl + e <= tl);
-                const bool strict = (i > j) || (sl + e < tl);
-                vq[e] = incl ? scale * aq[2 * hf + e] : 0.f;
-                vk[e] = strict ? bt * ak[2 * hf + e] : 0.f;
-                if (i == j) sLD[(i * 16 + tl) * 17 + sl + e] = vk[e];
+            for (int nt = 0; nt < 2; ++nt) {
+                const float *row = nt ? kbrow1 : kbrow0;
+                const float2 x0 = *reinterpret_cast<const float2 *>(row + c0);
+                const float2 x1 = *reinterpret_cast<const float2 *>(row + c0 + 8);
+                uint32_t bh0, bl0, bh1, bl1;
+                split_bf16(x0.x * f0.x, x0.y * f0.y, bh0, bl0);
+                split_bf16(x1.x * f1.x, x1.y * f1.y, bh1, bl1);
+                mma16816(aq[nt], fa, bh0, bh1);
+                mma16816(aq[nt], fl, bh0, bh1);
+                mma16816(aq[nt], fa, bl0, bl1);
+                mma16816(ak[nt], fk, bh0, bh1);
             }
-            *reinterpret_cast<uint32_t *>(sAqk + t * RSA + s) = pack_f16(vq[0], vq[1]);
-            *reinterpret_cast<uint32_t *>(sL + t * RSA + s) = pack_f16(vk[0], vk[1]);
         }
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                const int tl = gq + 8 * hf, sl = 8 * nt + 2 * qd;
+                const int t = 16 * i + tl, s = 16 * j + sl;
+                const float bt = sBeta[t];
+                float vq[2], vk[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const bool incl = (i > j) || (sl + e <= tl);
+                    const bool strict = (i > j) || (sl + e < tl);
+                    vq[e] = incl ? scale * aq[nt][2 * hf + e] : 0.f;
+                    vk[e] = strict ? bt * ak[nt][2 * hf + e] : 0.f;
+                    if (i == j) sLD[(i * 16 + tl) * 17 + sl + e] = vk[e];
+                }
+                *reinterpret_cast<uint32_t *>(sAqk + t * RSA + s) = pack_f16(vq[0], vq[1]);
+                *reinterpret_cast<uint32_t *>(sL + t * RSA + s) = pack_f16(vk[0], vk[1]);
+            }
     }
     // upper tiles of scale*Aqk are zero (the consumer reads the full 64x64)
     for (int idx = tid; idx < 6 * 16 * 8; idx += NCOMP) {
@@ -598,11 +606,8 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int pi
         KDA_TRACE_EV(p, 20, 0);
         unsigned char *slot = R.slots + static_cast<size_t>(cur.k * RING + s) * SLOT_BYTES;
         run_task(p, smem, slot, cur.ch, cur.c, vbuf, qlobuf, nxt, gate_bad, range_bad);
-        sync_compute();
-        if (tid == 0) {
-            __threadfence();
-            st_release(&R.ready[cur.k * RING + s], cur.j + 1);
-        }
+        sync_compute();  // every thread's slot stores precede the barrier, hence the release below
+        if (tid == 0) st_release(&R.ready[cur.k * RING + s], cur.j + 1);
         KDA_TRACE_EV(p, 3, cur.j * p.C + cur.k);
         cur = nxt;
         const int tmp = vbuf;
