@@ -48,7 +48,8 @@ typedef struct CUstream_st *kda_stream_t;
 typedef enum {
     KDA_OK = 0,
     KDA_ERR_INVALID_ARG = 1, /* null required pointer, bad size, misalignment, bad scalar */
-    KDA_ERR_UNSUPPORTED = 2, /* head_dim_k or head_dim_v other than 128 */
+    KDA_ERR_UNSUPPORTED = 2, /* head_dim_k or head_dim_v other than 128, or
+                                total_tokens above 2^31 - 65 */
     KDA_ERR_CUDA = 3,        /* a CUDA runtime call or the launch failed */
     KDA_ERR_GATE_RANGE = 4,  /* device: some g outside [lower_bound, 0] or not finite */
     KDA_ERR_BAD_SEQLENS = 5, /* device: cu_seqlens not 0 .. total_tokens nondecreasing */
@@ -73,6 +74,8 @@ typedef enum {
  *   q, k          bf16 [total_tokens, num_heads, 128]; k is expected to be
  *                 L2-normalised per (token, head) as in the model (not checked).
  *   v             bf16 [total_tokens, num_heads, 128].
+ *                 total_tokens may not exceed 2^31 - 65 (the tensor-copy
+ *                 coordinates of the input loads are 32-bit).
  *   g             fp32 [total_tokens, num_heads, 128]: natural-log decay per
  *                 key channel, already activated; lower_bound <= g <= 0.
  *   beta          fp32 [total_tokens, num_heads].

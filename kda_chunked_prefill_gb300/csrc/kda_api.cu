@@ -11,6 +11,7 @@ namespace {
 
 constexpr int32_t kVersion = 100;  // 0.1.0
 
+constexpr int64_t kKdaMaxTokens = 0x7fffffffLL - 64;
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // The strip products form factors up to 2^(8*|lower_bound|/ln 2); keep that
@@ -33,6 +34,7 @@ kda_status_t kda_chunk_fwd(const void *q, const void *k, const void *v, const fl
     if (static_cast<int64_t>(num_seqs) * num_heads > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
     if (total_tokens > (int64_t{1} << 40) / (static_cast<int64_t>(num_heads) * KDA_HEAD_DIM))
         return KDA_ERR_INVALID_ARG;
+    if (total_tokens > kKdaMaxTokens) return KDA_ERR_UNSUPPORTED;  // tensor-copy coordinates are 32-bit
     if (!(scale == scale) || !lower_bound_ok(lower_bound)) return KDA_ERR_INVALID_ARG;
     if (num_seqs == 0) return total_tokens == 0 ? KDA_OK : KDA_ERR_INVALID_ARG;
     if (!cu_seqlens || !aligned(cu_seqlens, 4)) return KDA_ERR_INVALID_ARG;

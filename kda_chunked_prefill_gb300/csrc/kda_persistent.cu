@@ -20,6 +20,11 @@
 // intra-chunk work (most of the arithmetic) is spread over every other SM.
 // All waits are bounded: a wait that runs out sets KDA_ERR_TIMEOUT and an abort
 // word in the workspace, and every CTA then returns.
+#include <cudaTypedefs.h>
+#include <string.h>
+
+#include <mutex>
+
 #include "kda.h"
 #include "kda_common.cuh"
 #include "kda_persistent.h"
@@ -31,6 +36,9 @@ constexpr int NCOMP = 512;            // 16 warps, all computing (<= 128 registe
 constexpr int NTHREADS = NCOMP;
 constexpr int NWARPS = NCOMP / 32;
 constexpr long long SPIN_LIMIT = 1ll << 24;
+#ifdef KDA_TRACE
+constexpr int TRACE_COUNTS_OFFSET = 231424;  // past every role's tiles (checked below), 16 ints
+#endif
 
 // ---------------------------------------------------------------- slot layout
 // A slot holds one (chain, chunk) hand-off; every region is 1024-byte aligned.
@@ -67,26 +75,39 @@ __device__ __forceinline__ int at_addr(int lane, int rows, int m0, int k0) {  //
 
 __device__ __forceinline__ void sync_compute() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
 
-// Optional event trace (compiled in only with -DKDA_TRACE): per CTA, up to
-// TRACE_EVENTS records {globaltimer ns, tag, value} after the ring in the workspace.
+// Optional event trace (compiled in only with -DKDA_TRACE): per CTA and warp,
+// up to TRACE_EVENTS records {globaltimer ns, tag << 32 | value} after the ring
+// in the workspace, written by lane 0 of the warp; per-warp counts live in
+// shared memory (past the roles' tiles) and are mirrored to the workspace.
 #ifdef KDA_TRACE
 constexpr int TRACE_EVENTS = 512;
-__device__ __forceinline__ void trace(const Params &p, int tag, int value) {
-    if (threadIdx.x != 0) return;
+constexpr size_t TRACE_CTA_WORDS = 16 + 16 * TRACE_EVENTS * 2;
+__device__ __forceinline__ void trace_any(const Params &p, int tag, int value) {
+    extern __shared__ unsigned char smem_raw[];
+    int *cnt = reinterpret_cast<int *>(smem_raw + TRACE_COUNTS_OFFSET);
     unsigned long long t;
     asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    const int w = threadIdx.x >> 5;
     unsigned char *base = p.ws + ring_offset(p.C) + static_cast<size_t>(p.C) * RING * SLOT_BYTES;
-    unsigned long long *rec = reinterpret_cast<unsigned long long *>(base) + blockIdx.x * (TRACE_EVENTS * 2 + 1);
-    const unsigned long long n = rec[0];
+    unsigned long long *rec = reinterpret_cast<unsigned long long *>(base) + blockIdx.x * TRACE_CTA_WORDS;
+    const int n = cnt[w];
     if (n < TRACE_EVENTS) {
-        rec[1 + 2 * n] = t;
-        rec[2 + 2 * n] = (static_cast<unsigned long long>(tag) << 32) | static_cast<unsigned>(value);
-        rec[0] = n + 1;
+        unsigned long long *r = rec + 16 + (static_cast<size_t>(w) * TRACE_EVENTS + n) * 2;
+        r[0] = t;
+        r[1] = (static_cast<unsigned long long>(tag) << 32) | static_cast<unsigned>(value);
+        cnt[w] = n + 1;
+        rec[w] = n + 1;
     }
 }
+__device__ __forceinline__ void trace(const Params &p, int tag, int value) {
+    if (threadIdx.x != 0) return;
+    trace_any(p, tag, value);
+}
 #define KDA_TRACE_EV(p, tag, value) trace(p, tag, value)
+#define KDA_TRACE_ANY(p, tag, value) trace_any(p, tag, value)
 #else
 #define KDA_TRACE_EV(p, tag, value) ((void)0)
+#define KDA_TRACE_ANY(p, tag, value) ((void)0)
 #endif
 
 // ---------------------------------------------------------------- workspace
@@ -134,10 +155,20 @@ __device__ __forceinline__ bool wait_mbar(const Ring &R, uint64_t *bar, uint32_t
     return false;
 }
 
-// chunks of chain ch (sequence ch / H), or -1 when its bounds are invalid
-__device__ __forceinline__ int chain_info(const Params &p, int ch, int64_t &bos, int64_t &len) {
+// After an abort: wait (bounded, ignoring the abort word) for this CTA's own
+// bulk copies on `bar` to land before it leaves.
+__device__ __forceinline__ void drain_mbar(uint64_t *bar, uint32_t parity) {
+    for (long long it = 0; it < SPIN_LIMIT; ++it) {
+        if (mbar_try_wait(bar, parity)) return;
+        __nanosleep(64);
+    }
+}
+
+// chunks of chain ch (sequence ch / H), or -1 when its bounds are invalid;
+// `cu` is p.cu or a copy of it in shared memory
+__device__ __forceinline__ int chain_info(const Params &p, const int32_t *cu, int ch, int64_t &bos, int64_t &len) {
     const int n = ch / p.H;
-    const int64_t b = p.cu[n], e = p.cu[n + 1];
+    const int64_t b = cu[n], e = cu[n + 1];
     const bool bad = b < 0 || e < b || e > p.T || (n == 0 && b != 0) || (n == p.N - 1 && e != p.T);
     if (bad) {
         bos = 0;
@@ -150,24 +181,27 @@ __device__ __forceinline__ int chain_info(const Params &p, int ch, int64_t &bos,
 }
 
 // consumer k owns chains k, k + C, k + 2C, ...; its chunks form one sequence
-__device__ __forceinline__ int consumer_total(const Params &p, int k) {
+__device__ __forceinline__ int consumer_total(const Params &p, const int32_t *cu, int k) {
     int tot = 0;
     for (int ch = k; ch < p.N * p.H; ch += p.C) {
         int64_t b, l;
-        const int nc = chain_info(p, ch, b, l);
+        const int nc = chain_info(p, cu, ch, b, l);
         tot += nc > 0 ? nc : 0;
     }
     return tot;
 }
 
-__device__ __forceinline__ bool map_task(const Params &p, int k, int j, int &ch_out, int &c_out) {
+__device__ __forceinline__ bool map_task(const Params &p, const int32_t *cu, int k, int j, int &ch_out, int &c_out,
+                                         int64_t &bos, int64_t &len) {
     for (int ch = k; ch < p.N * p.H; ch += p.C) {
         int64_t b, l;
-        int nc = chain_info(p, ch, b, l);
+        int nc = chain_info(p, cu, ch, b, l);
         if (nc < 0) nc = 0;
         if (j < nc) {
             ch_out = ch;
             c_out = j;
+            bos = b;
+            len = l;
             return true;
         }
         j -= nc;
@@ -176,122 +210,208 @@ __device__ __forceinline__ bool map_task(const Params &p, int k, int j, int &ch_
 }
 
 // ================================================================== producer
-// Steps 1-4 for one (chain, chunk) task at a time, on 256 threads with
-// warp-level tensor-core products (m16n8k16) for the 16x16 tiles.
+// Steps 1-4 for one (chain, chunk) task at a time on all sixteen warps, with
+// warp-level tensor-core products (m16n8k16) for the 16x16 tiles. The task's
+// ring slot is assembled in shared memory (the slot image) and leaves with one
+// bulk store; while warps 0-9 compute the strips, one thread of the idle last
+// warp publishes the previous slot, draws the next task and waits for this
+// task's slot to be free, so none of that memory traffic stalls the warps.
 namespace prod {
-constexpr int RSB = 136, RSF = 136, RSA = 72, RSI = 24;
-constexpr int SZ_T = BT * RSB * 2;        // 17408
-constexpr int SZ_F = BT * RSF * 4;        // 34816
-constexpr int OFF_Q = 0;                  // q -> q*a (bf16 hi)
-constexpr int OFF_QLO = OFF_Q + SZ_T;     // q*a (bf16 lo); v / u of the next task (roles swap per task)
-constexpr int OFF_K = OFF_QLO + SZ_T;     // k -> k*a (bf16)
-constexpr int OFF_V = OFF_K + SZ_T;       // v -> beta*v -> u (fp16); q*a lo of the next task
-constexpr int OFF_RK = OFF_V + SZ_T;      // beta*k*e^G -> w (fp16)
-constexpr int OFF_G = OFF_RK + SZ_T;      // g -> G (fp32)
-constexpr int OFF_KB = OFF_G + SZ_F;      // k*e^(G_m - G) (fp32)
-constexpr int OFF_AQK = OFF_KB + SZ_F;    // scale*Aqk (fp16 [64][RSA])
-constexpr int SZ_A = BT * RSA * 2;        // 9216
-constexpr int OFF_L = OFF_AQK + SZ_A;     // L (fp16 [64][RSA])
-constexpr int OFF_LD = OFF_L + SZ_A;      // diagonal blocks of L, fp32 [4][16][17]
-constexpr int OFF_INV = OFF_LD + 4352;    // (I+L_ii)^-1 fp16 [4][16][RSI]
-constexpr int OFF_TAB = OFF_INV + 3072;   // per-channel tables, fp32 [20][128]
+// q, k, v and their derived tiles are [64 tokens][128 channels] 16-bit tiles
+// and g is a [64][128] fp32 tile, all in the 128-byte-swizzled layout the
+// tensor copies write (16 KB and 32 KB; 1024-byte aligned).
+constexpr int RSF = 136, RSA = 72;
+constexpr int SZ_T = BT * DK * 2;             // 16384
+constexpr int SZ_F = BT * RSF * 4;            // 34816 (kb keeps a padded row stride)
+constexpr int OFF_IMG = 0;                    // slot image: the bytes of one ring slot
+constexpr int OFF_Q = OFF_IMG + SLOT_BYTES;   // q; then q*a as tf32 (fp32 [64][128], spans OFF_Q and OFF_QLO)
+constexpr int OFF_QLO = OFF_Q + SZ_T;
+constexpr int OFF_K = OFF_QLO + SZ_T;         // k -> k*a (bf16)
+constexpr int OFF_V = OFF_K + SZ_T;           // v (bf16)
+constexpr int OFF_GKB = OFF_V + SZ_T;         // g -> G (fp32, swizzled), then k*e^(G_m - G) (fp32, padded)
+constexpr int SZ_A = BT * RSA * 2;            // 9216
+constexpr int OFF_L = OFF_GKB + SZ_F;         // L (fp16 [64][RSA])
+constexpr int OFF_LD = OFF_L + SZ_A;          // diagonal blocks of L, fp32 [4][16][17]
+constexpr int OFF_T = OFF_LD + 4352;          // T = (I+L)^-1, fp16 [64][RSA] (lower blocks)
+constexpr int OFF_TAB = OFF_T + SZ_A;         // per-channel tables, fp32 [20][128]
 constexpr int OFF_BETA = OFF_TAB + 10240;
-constexpr int OFF_MISC = OFF_BETA + 256;  // flags and the task broadcast
-constexpr int SMEM = OFF_MISC + 64;
+constexpr int OFF_MISC = OFF_BETA + 256;      // flags and the task broadcast (32 ints)
+constexpr int OFF_BAR = OFF_MISC + 128;       // input-load mbarriers: g, then q/k/v
+constexpr int OFF_CU = OFF_BAR + 16;          // copy of cu_seqlens when it has at most CU_CACHE entries
+constexpr int CU_CACHE = 1024;
+constexpr int SMEM = OFF_CU + 4 * CU_CACHE;
+constexpr int SYNC_TID = NCOMP - 32;          // lane 0 of warp 15: draws tasks, waits for free slots
+constexpr int REL_TID = NCOMP - 64;           // lane 0 of warp 14: stores slot images and publishes them
 constexpr int TGM = 0, TGL = 4 * 128, TEM = 5 * 128, TEL = 9 * 128, TF = 13 * 128, TD = 19 * 128;
+static_assert(OFF_Q % 1024 == 0 && OFF_GKB % 1024 == 0, "tensor-copy destinations are 1024-byte aligned");
+// byte offset of the 16-byte chunk holding channels [c4, c4+4) of row r of the g tile
+__device__ __forceinline__ int g_chunk(int r, int c4) {
+    return (c4 >> 5) * (BT * 128) + r * 128 + ((((c4 >> 2) & 7) ^ (r & 7)) << 4);
+}
+__device__ __forceinline__ int g_elem(int r, int c) { return g_chunk(r, c & ~3) + ((c & 3) << 2); }
+// q*a tile, fp32 [64][128]: channel pair c/2 of row r is stored at pair
+// (c/2) ^ 4(r mod 4), so the strip loads (8 bytes at rows g, channels 2q + 16k)
+// are free of bank conflicts and a group of 4 pairs stays 32 contiguous bytes
+__device__ __forceinline__ int qa_pair(int r, int c) { return r * 512 + ((((c >> 1) ^ ((r & 3) << 2))) << 3); }
 __device__ __forceinline__ int f_pair(int i, int j) { return i * (i - 1) / 2 + j; }
 __device__ __forceinline__ bool f16_ok(float x) { return fabsf(x) < F16_SAFE; }
+// The image leaves in two bulk stores: q_hat (rows 0-63 of A1) and kg as soon
+// as the elementwise step has written them, the rest after the solve.
+__device__ __forceinline__ void store_early(unsigned char *dst, const unsigned char *img) {
+    fence_proxy_async_global();  // after the acquire that found the slot free
+    bulk_s2g(dst + SL_A1, img + SL_A1, 8192);                  // q_hat, channels 0-63
+    bulk_s2g(dst + SL_A1 + 16384, img + SL_A1 + 16384, 8192);  // q_hat, channels 64-127
+    bulk_s2g(dst + SL_KG, img + SL_KG, SL_U - SL_KG);          // kg
+    bulk_commit();
+}
+__device__ __forceinline__ void store_late(unsigned char *dst, const unsigned char *img) {
+    bulk_s2g(dst + SL_A1 + 8192, img + SL_A1 + 8192, 8192);    // w, channels 0-63
+    bulk_s2g(dst + SL_A1 + 24576, img + SL_A1 + 24576, 8192);  // w, channels 64-127
+    bulk_s2g(dst + SL_U, img + SL_U, SLOT_BYTES - SL_U);       // u, e^(G_last), scale*Aqk
+    bulk_commit();
+}
+static_assert(SL_KG == 32768 && SL_U == 49152 && SL_D == 65536 && SL_AQK > SL_D, "slot layout used by the stores");
 
-// One (chain, chunk) task: steps 1-4, results into the global slot.
+// slot-image byte offsets of u (token rows of U) and w (rows 64-127 of A1)
+__device__ __forceinline__ int uw_chunk(bool isw, int r, int c8) {
+    return isw ? SL_A1 + tile_chunk(128, 64 + r, c8) : SL_U + tile_chunk(64, r, c8);
+}
+__device__ __forceinline__ int uw_elem(bool isw, int r, int c) { return uw_chunk(isw, r, c & ~7) + ((c & 7) << 1); }
+__device__ __forceinline__ int uw_bk(bool isw, int lane, int k0, int n0) {  // ldmatrix.trans lane address, B [k][n]
+    return isw ? SL_A1 + bk_addr(lane, 128, 64 + k0, n0) : SL_U + bk_addr(lane, 64, k0, n0);
+}
+
+// A task and where its tokens are: t0 = first token of the chunk, nv = its
+// valid rows (computed once when the task is drawn, so that no later step
+// reads the sequence bounds from global memory again).
 struct Task {
-    int valid, k, j, ch, c;
+    int valid, k, j, ch, c, t0, nv;
 };
+__device__ __forceinline__ void put_task(int *m, const Task &t) {
+    m[0] = t.valid; m[1] = t.k; m[2] = t.j; m[3] = t.ch; m[4] = t.c; m[5] = t.t0; m[6] = t.nv;
+}
+__device__ __forceinline__ Task get_task(const int *m) { return Task{m[0], m[1], m[2], m[3], m[4], m[5], m[6]}; }
 
-// next valid task (thread 0): tasks are numbered j * C + k so every consumer advances together
-__device__ __forceinline__ Task fetch_task(const Params &p, const Ring &R, int jmax) {
-    Task t{0, 0, 0, 0, 0};
-    while (true) {
-        const int task = atomicAdd(&R.hdr->counter, 1);
-        t.k = task % p.C;
-        t.j = task / p.C;
-        if (t.j >= jmax) return t;
-        if (map_task(p, t.k, t.j, t.ch, t.c)) {
+// Tasks are numbered j * C + k (chunk j of consumer k), so every consumer
+// advances together; producer pid takes the numbers pid, pid + P, pid + 2P,
+// ... in order. The cursor holds the next number as (k, j) and the stride P
+// as (P mod C, P div C), so that drawing divides nothing.
+struct Cursor {
+    int k, j, dk, dj;
+};
+__device__ __forceinline__ Cursor make_cursor(int pid, int P, int C) { return Cursor{pid % C, pid / C, P % C, P / C}; }
+
+// next valid task of the cursor (numbers whose consumer has fewer chunks are skipped)
+__device__ __forceinline__ Task fetch_task(const Params &p, const int32_t *cu, int jmax, Cursor &cs) {
+    Task t{0, 0, 0, 0, 0, 0, 0};
+    while (cs.j < jmax) {
+        t.k = cs.k;
+        t.j = cs.j;
+        cs.k += cs.dk;
+        cs.j += cs.dj;
+        if (cs.k >= p.C) {
+            cs.k -= p.C;
+            ++cs.j;
+        }
+        int64_t bos, len;
+        if (map_task(p, cu, t.k, t.j, t.ch, t.c, bos, len)) {
+            const int64_t t0 = bos + static_cast<int64_t>(t.c) * BT;
+            t.t0 = static_cast<int>(t0);
+            t.nv = static_cast<int>((bos + len - t0) < BT ? (bos + len - t0) : BT);
             t.valid = 1;
             return t;
         }
     }
+    return t;
 }
 
-// cp.async of part of one task's inputs (rows >= nv zero-filled):
-// part 0: g; part 1: q, k, v (v into vbuf) and beta.
-__device__ __forceinline__ void issue_loads(const Params &p, unsigned char *smem, const Task &tk, int part, int vbuf) {
+// One task's inputs into shared memory, called by all threads once the
+// buffers are free: q, k, v and g as ten tiled tensor copies issued by
+// SYNC_TID, g completing on `bar_g` and q, k, v on `bar_q` (one phase per
+// task each, so the prefix sum can start before q, k, v land), beta by cp.async.
+// Rows past the sequence end are zeroed once the copies have landed.
+__device__ __forceinline__ void issue_loads(const Params &p, unsigned char *smem, const Task &tk, uint64_t *bar_g,
+                                            uint64_t *bar_q) {
     const int tid = threadIdx.x;
     const int h = tk.ch % p.H;
-    int64_t bos, len;
-    chain_info(p, tk.ch, bos, len);
-    const int64_t t0 = bos + static_cast<int64_t>(tk.c) * BT;
-    const int nv = static_cast<int>((bos + len - t0) < BT ? (bos + len - t0) : BT);
-    const size_t rs = static_cast<size_t>(p.H) * DK;
-    const size_t base = (static_cast<size_t>(t0) * p.H + h) * DK;
-    if (part == 0) {
-        float *sG = reinterpret_cast<float *>(smem + OFF_G);
-        for (int idx = tid; idx < BT * 32; idx += NCOMP) {
-            const int r = idx >> 5, c4 = (idx & 31) << 2;
-            const bool ok = r < nv;
-            cp_async16(sG + r * RSF + c4, p.g + base + (ok ? r * rs : 0) + c4, ok ? 16 : 0);
+    const int64_t t0 = tk.t0;
+    const int nv = tk.nv;
+    if (tid == SYNC_TID) {
+        const int z = tk.t0;
+        mbar_arrive_expect_tx(bar_g, BT * DK * 4);
+        for (int qt = 0; qt < 4; ++qt) tma_load_3d(smem + OFF_GKB + qt * (BT * 128), &p.tm_g, 32 * qt, h, z, bar_g);
+        mbar_arrive_expect_tx(bar_q, 3 * SZ_T);
+        for (int half = 0; half < 2; ++half) {
+            tma_load_3d(smem + OFF_Q + half * (SZ_T / 2), &p.tm_q, 64 * half, h, z, bar_q);
+            tma_load_3d(smem + OFF_K + half * (SZ_T / 2), &p.tm_k, 64 * half, h, z, bar_q);
+            tma_load_3d(smem + OFF_V + half * (SZ_T / 2), &p.tm_v, 64 * half, h, z, bar_q);
         }
-    } else {
-        __nv_bfloat16 *sQ = reinterpret_cast<__nv_bfloat16 *>(smem + OFF_Q);
-        __nv_bfloat16 *sK = reinterpret_cast<__nv_bfloat16 *>(smem + OFF_K);
-        __nv_bfloat16 *sV = reinterpret_cast<__nv_bfloat16 *>(smem + vbuf);
-        for (int idx = tid; idx < BT * 16; idx += NCOMP) {
-            const int r = idx >> 4, c8 = (idx & 15) << 3;
-            const bool ok = r < nv;
-            const size_t off = base + (ok ? r * rs : 0) + c8;
-            cp_async16(sQ + r * RSB + c8, p.q + off, ok ? 16 : 0);
-            cp_async16(sK + r * RSB + c8, p.k + off, ok ? 16 : 0);
-            cp_async16(sV + r * RSB + c8, p.v + off, ok ? 16 : 0);
-        }
-        if (tid < BT) {
-            const bool ok = tid < nv;
-            cp_async4(smem + OFF_BETA + 4 * tid, p.beta + static_cast<size_t>(t0 + (ok ? tid : 0)) * p.H + h, ok ? 4 : 0);
-        }
+        KDA_TRACE_ANY(p, 30, 0);
+    }
+    if (tid < BT) {
+        const bool ok = tid < nv;
+        cp_async4(smem + OFF_BETA + 4 * tid, p.beta + static_cast<size_t>(t0 + (ok ? tid : 0)) * p.H + h, ok ? 4 : 0);
     }
     cp_async_commit();
 }
 
-// One (chain, chunk) task: steps 1-4, results into the global slot. Its inputs
-// were loaded by issue_loads; `vbuf` holds v (then u), `qlobuf` receives q*a lo
-// and then the next task's v. `nxt` (valid or not) is loaded as buffers free up.
-__device__ __forceinline__ void run_task(const Params &p, unsigned char *smem, unsigned char *slot, int ch, int c,
-                                         int vbuf, int qlobuf, const Task &nxt, bool &gate_bad, bool &range_bad) {
-    __nv_bfloat16 *sQ = reinterpret_cast<__nv_bfloat16 *>(smem + OFF_Q);
-    __nv_bfloat16 *sQlo = reinterpret_cast<__nv_bfloat16 *>(smem + qlobuf);
-    __nv_bfloat16 *sK = reinterpret_cast<__nv_bfloat16 *>(smem + OFF_K);
-    __nv_bfloat16 *sV = reinterpret_cast<__nv_bfloat16 *>(smem + vbuf);
-    __half *sRV = reinterpret_cast<__half *>(smem + vbuf);
-    __half *sRK = reinterpret_cast<__half *>(smem + OFF_RK);
-    float *sG = reinterpret_cast<float *>(smem + OFF_G);
-    float *sKB = reinterpret_cast<float *>(smem + OFF_KB);
-    __half *sAqk = reinterpret_cast<__half *>(smem + OFF_AQK);
+// rows >= nv of the input tiles (the tensor copies read the next sequence
+// there): zero, so that padded tokens contribute nothing and g = 0 keeps
+// row 63 of G at the last valid prefix
+__device__ __forceinline__ void zero_tail(unsigned char *smem, const Task &tk) {
+    const int nv = tk.nv;
+    for (int idx = nv * 8 + threadIdx.x; idx < BT * 8; idx += NCOMP) {  // whole 128-byte rows
+        const int r = idx >> 3, c = (idx & 7) << 4;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const int off = half * (SZ_T / 2) + r * 128 + c;
+            *reinterpret_cast<uint4 *>(smem + OFF_Q + off) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4 *>(smem + OFF_K + off) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4 *>(smem + OFF_V + off) = make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int qt = 0; qt < 4; ++qt)
+            *reinterpret_cast<uint4 *>(smem + OFF_GKB + qt * (BT * 128) + r * 128 + c) = make_uint4(0, 0, 0, 0);
+    }
+}
+
+// One (chain, chunk) task: steps 1-4 into the slot image, then the bulk store
+// of the image into the task's slot. Its inputs were loaded by issue_loads.
+// `nxt` is the next task (drawn one task earlier); its tensor copies start
+// right after the strips.
+// During the strips, REL_TID completes and publishes the previous task's slot
+// (`pending` = its ready-flag index or -1, `pending_val` the value) while
+// SYNC_TID draws the task after `nxt` into `nxt2` and waits for this task's
+// slot to be free. The publication waits only for this CTA's own bulk store,
+// never for a consumer, so a producer never waits on a consumer while its
+// finished chunk stays unpublished (and tasks drawn but not started wait on
+// nothing: the lowest-numbered unpublished task can always proceed).
+// Returns false when the slot wait gave up (timeout or abort).
+__device__ __forceinline__ bool run_task(const Params &p, const Ring &Rg, unsigned char *smem, const Task &cur,
+                                         const int32_t *cu_s, int jmax, const Task &nxt, Task &nxt2, Cursor &cs, int &pending,
+                                         int pending_val, uint64_t *bar_g, uint64_t *bar_q, uint32_t ph,
+                                         int &landed_q, int &issued, bool &gate_bad, bool &range_bad) {
+    unsigned char *img = smem + OFF_IMG;
+    unsigned char *sQ = smem + OFF_Q, *sK = smem + OFF_K, *sV = smem + OFF_V;
+    unsigned char *sGb = smem + OFF_GKB;  // G, swizzled (g_chunk / g_elem)
+    float *sKB = reinterpret_cast<float *>(smem + OFF_GKB);
     __half *sL = reinterpret_cast<__half *>(smem + OFF_L);
     float *sLD = reinterpret_cast<float *>(smem + OFF_LD);
-    __half *sInv = reinterpret_cast<__half *>(smem + OFF_INV);
+    __half *sT = reinterpret_cast<__half *>(smem + OFF_T);
     float *sTab = reinterpret_cast<float *>(smem + OFF_TAB);
     float *sBeta = reinterpret_cast<float *>(smem + OFF_BETA);
+    int *misc = reinterpret_cast<int *>(smem + OFF_MISC);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int gq = lane >> 2, qd = lane & 3;
     const float scale = p.scale;
-    (void)ch;
-    (void)c;
     // ---- step 1: inclusive prefix sum of g (base 2) per key channel, four
     // 16-row quarters per channel on all 512 threads, then the per-channel tables
     {
         const int chn = tid & 127, rq = tid >> 7;
         float x[16];
 #pragma unroll
-        for (int q = 0; q < 16; ++q) x[q] = sG[(16 * rq + q) * RSF + chn];
+        for (int q = 0; q < 16; ++q) x[q] = *reinterpret_cast<const float *>(sGb + g_elem(16 * rq + q, chn));
         float acc = 0.f;
         bool gb = false;
 #pragma unroll
@@ -306,15 +426,15 @@ __device__ __forceinline__ void run_task(const Params &p, unsigned char *smem, u
         float cy = 0.f;
         for (int q = 0; q < rq; ++q) cy += sTab[TEM + q * 128 + chn];
 #pragma unroll
-        for (int q = 0; q < 16; ++q) sG[(16 * rq + q) * RSF + chn] = x[q] + cy;
+        for (int q = 0; q < 16; ++q) *reinterpret_cast<float *>(sGb + g_elem(16 * rq + q, chn)) = x[q] + cy;
     }
     sync_compute();
     if (tid < DK) {  // rows >= nv carry g = 0, so row 63 holds the last valid prefix
         const int chn = tid;
         float gm[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) gm[i] = sG[(16 * i + 7) * RSF + chn];
-        const float gl = sG[63 * RSF + chn];
+        for (int i = 0; i < 4; ++i) gm[i] = *reinterpret_cast<const float *>(sGb + g_elem(16 * i + 7, chn));
+        const float gl = *reinterpret_cast<const float *>(sGb + g_elem(63, chn));
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             sTab[TGM + i * 128 + chn] = gm[i];
@@ -328,24 +448,32 @@ __device__ __forceinline__ void run_task(const Params &p, unsigned char *smem, u
 #pragma unroll
             for (int j = 0; j < i; ++j) sTab[TF + f_pair(i, j) * 128 + chn] = ex2(gm[i] - gm[j]);
     }
-    sync_compute();
+    if (tid == REL_TID) bulk_wait_read();  // the previous image has been read out and may be rewritten
+    const bool q_landed = wait_mbar(Rg, bar_q, ph, p.status);
+    if (__syncthreads_or(!q_landed)) return false;  // one decision for the whole CTA
+    ++landed_q;
     KDA_TRACE_EV(p, 21, 0);
 
-    // ---- steps 2a/4a: elementwise operands; q_hat and kg go straight to the slot
+    // ---- steps 2a/4a: elementwise operands; q_hat, kg, beta*v and
+    // beta*k*e^G go straight into the slot image
     {
         // thread: channels c8..c8+7 of rows r0 and r0 + 8, both in sub-block i
         const int ew_i = tid >> 7, ew_c8 = (tid & 15) << 3, ew_r0 = 16 * ew_i + ((tid >> 4) & 7);
         float Gv[2][8];
+        uint4 qv[2], kv[2], vv[2];
 #pragma unroll
         for (int it = 0; it < 2; ++it) {
             const int r = ew_r0 + 8 * it, c8 = ew_c8;
-            const float4 a = *reinterpret_cast<const float4 *>(sG + r * RSF + c8);
-            const float4 b = *reinterpret_cast<const float4 *>(sG + r * RSF + c8 + 4);
+            const float4 a = *reinterpret_cast<const float4 *>(sGb + g_chunk(r, c8));
+            const float4 b = *reinterpret_cast<const float4 *>(sGb + g_chunk(r, c8 + 4));
             Gv[it][0] = a.x; Gv[it][1] = a.y; Gv[it][2] = a.z; Gv[it][3] = a.w;
             Gv[it][4] = b.x; Gv[it][5] = b.y; Gv[it][6] = b.z; Gv[it][7] = b.w;
+            const int tc = tile_chunk(64, r, c8);
+            qv[it] = *reinterpret_cast<const uint4 *>(sQ + tc);
+            kv[it] = *reinterpret_cast<const uint4 *>(sK + tc);
+            vv[it] = *reinterpret_cast<const uint4 *>(sV + tc);
         }
-        sync_compute();  // the gate tile is free from here on: stream in the next task's g
-        if (nxt.valid) issue_loads(p, smem, nxt, 0, 0);
+        sync_compute();  // G and q are read: kb and q*a overwrite them below
         float GM[8], EM[8], EL[8];
         {
             const int i = ew_i, c8 = ew_c8;
@@ -363,13 +491,11 @@ __device__ __forceinline__ void run_task(const Params &p, unsigned char *smem, u
         for (int it = 0; it < 2; ++it) {
             const int r = ew_r0 + 8 * it, c8 = ew_c8;
             const float bt = sBeta[r];
-            const uint4 qv = *reinterpret_cast<const uint4 *>(sQ + r * RSB + c8);
-            const uint4 kv = *reinterpret_cast<const uint4 *>(sK + r * RSB + c8);
-            const uint4 vv = *reinterpret_cast<const uint4 *>(sV + r * RSB + c8);
-            const uint32_t *qw = reinterpret_cast<const uint32_t *>(&qv);
-            const uint32_t *kw = reinterpret_cast<const uint32_t *>(&kv);
-            const uint32_t *vw = reinterpret_cast<const uint32_t *>(&vv);
-            uint32_t oQh[4], oQl[4], oKa[4], oBv[4], oBk[4], oQs[4], oKg[4];
+            const int tc = tile_chunk(64, r, c8);
+            const uint32_t *qw = reinterpret_cast<const uint32_t *>(&qv[it]);
+            const uint32_t *kw = reinterpret_cast<const uint32_t *>(&kv[it]);
+            const uint32_t *vw = reinterpret_cast<const uint32_t *>(&vv[it]);
+            uint32_t oQa[8], oKa[4], oBv[4], oBk[4], oQs[4], oKg[4];
             float kb[8];
 #pragma unroll
             for (int q2 = 0; q2 < 4; ++q2) {
@@ -390,7 +516,8 @@ __device__ __forceinline__ void run_task(const Params &p, unsigned char *smem, u
                     res[e][5] = kk * b * EL[ce];   // k e^(G_last - G)
                     kb[ce] = kk * b;               // k e^(G_m - G)
                 }
-                split_bf16(res[0][0], res[1][0], oQh[q2], oQl[q2]);
+                oQa[2 * q2] = to_tf32(res[0][0]);
+                oQa[2 * q2 + 1] = to_tf32(res[1][0]);
                 oKa[q2] = pack_bf16(res[0][1], res[1][1]);
                 range_bad |= !(f16_ok(res[0][2]) && f16_ok(res[1][2]));
                 oBv[q2] = pack_f16(res[0][2], res[1][2]);
@@ -398,23 +525,54 @@ __device__ __forceinline__ void run_task(const Params &p, unsigned char *smem, u
                 oQs[q2] = pack_f16(res[0][4], res[1][4]);
                 oKg[q2] = pack_f16(res[0][5], res[1][5]);
             }
-            *reinterpret_cast<uint4 *>(sQ + r * RSB + c8) = *reinterpret_cast<uint4 *>(oQh);
-            *reinterpret_cast<uint4 *>(sQlo + r * RSB + c8) = *reinterpret_cast<uint4 *>(oQl);
-            *reinterpret_cast<uint4 *>(sK + r * RSB + c8) = *reinterpret_cast<uint4 *>(oKa);
-            *reinterpret_cast<uint4 *>(sRV + r * RSB + c8) = *reinterpret_cast<uint4 *>(oBv);
-            *reinterpret_cast<uint4 *>(sRK + r * RSB + c8) = *reinterpret_cast<uint4 *>(oBk);
+            *reinterpret_cast<uint4 *>(sQ + qa_pair(r, c8)) = make_uint4(oQa[0], oQa[1], oQa[2], oQa[3]);
+            *reinterpret_cast<uint4 *>(sQ + qa_pair(r, c8) + 16) = make_uint4(oQa[4], oQa[5], oQa[6], oQa[7]);
+            *reinterpret_cast<uint4 *>(sK + tc) = *reinterpret_cast<uint4 *>(oKa);
             *reinterpret_cast<float4 *>(sKB + r * RSF + c8) = make_float4(kb[0], kb[1], kb[2], kb[3]);
             *reinterpret_cast<float4 *>(sKB + r * RSF + c8 + 4) = make_float4(kb[4], kb[5], kb[6], kb[7]);
-            *reinterpret_cast<uint4 *>(slot + SL_A1 + tile_chunk(128, r, c8)) = *reinterpret_cast<uint4 *>(oQs);
-            *reinterpret_cast<uint4 *>(slot + SL_KG + tile_chunk(64, r, c8)) = *reinterpret_cast<uint4 *>(oKg);
+            *reinterpret_cast<uint4 *>(img + uw_chunk(false, r, c8)) = *reinterpret_cast<uint4 *>(oBv);
+            *reinterpret_cast<uint4 *>(img + uw_chunk(true, r, c8)) = *reinterpret_cast<uint4 *>(oBk);
+            *reinterpret_cast<uint4 *>(img + SL_A1 + tile_chunk(128, r, c8)) = *reinterpret_cast<uint4 *>(oQs);
+            *reinterpret_cast<uint4 *>(img + SL_KG + tile_chunk(64, r, c8)) = *reinterpret_cast<uint4 *>(oKg);
         }
+        if (tid < 32)
+            *reinterpret_cast<float4 *>(img + SL_D + 16 * tid) = *reinterpret_cast<const float4 *>(sTab + TD + 4 * tid);
     }
+    // the image parts just written are read by the early bulk store, and the
+    // input tiles just written (q*a, k*a, kb) are rewritten by the next tensor
+    // copies: order these generic writes before both
+    fence_proxy_async_shared();
     sync_compute();
     KDA_TRACE_EV(p, 22, 0);
 
-    // ---- step 2b: Aqk (split bf16, three products) and Akk (bf16) on the 10
-    // lower 16x16 tiles. Tile (i,j) needs k_s e^(G_{m_i} - G_s) for s in
-    // sub-block j: the stored k e^(G_{m_j} - G) times e^(G_{m_i} - G_{m_j}) (<= 1).
+    // ---- ring work, on warps 14 and 15 (no strip pair, no diagonal block).
+    // REL_TID: publish the previous slot, then wait for this task's slot and
+    // send the part of the image that is final already. SYNC_TID: draw.
+    unsigned char *dst = Rg.slots + static_cast<size_t>(cur.k * RING + cur.j % RING) * SLOT_BYTES;
+    if (tid == REL_TID) {
+        if (pending >= 0) {
+            bulk_wait_all();
+            fence_proxy_async_global();
+            st_release(&Rg.ready[pending], pending_val);
+            pending = -1;
+        }
+        KDA_TRACE_ANY(p, 31, 0);
+        const int s = cur.j % RING;
+        const bool free_ok =
+            (cur.j < RING) || wait_flag_geq(Rg, &Rg.freed[cur.k * RING + s], cur.j - RING + 1, p.status);
+        misc[9] = free_ok ? 1 : 0;
+        if (free_ok) store_early(dst, img);
+        KDA_TRACE_ANY(p, 33, 0);
+    }
+    if (tid == SYNC_TID) {
+        const Task t = fetch_task(p, cu_s, jmax, cs);
+        put_task(misc + 2, t);
+        KDA_TRACE_ANY(p, 35, 0);
+    }
+    // ---- step 2b: Aqk (tf32) and Akk (bf16) on the 10
+    // lower 16x16 tiles, one tile per warp. Tile (i,j) needs k_s e^(G_{m_i} - G_s)
+    // for s in sub-block j: the stored k e^(G_{m_j} - G) times e^(G_{m_i} - G_{m_j}) (<= 1).
+    static_assert(NWARPS == 16, "warps 0-9 strips, 10-13 diagonal inverses, 14-15 ring work");
     for (int pair = warp; pair < 10; pair += NWARPS) {
         int i = 0;
         while ((i + 1) * (i + 2) / 2 <= pair) ++i;
@@ -423,13 +581,23 @@ __device__ __forceinline__ void run_task(const Params &p, unsigned char *smem, u
         const float *kbrow1 = sKB + (16 * j + 8 + gq) * RSF;  // column s = 16j + 8 + gq
         const float *fr = sTab + TF + (i > j ? f_pair(i, j) : 0) * 128;
         float aq[2][4] = {}, ak[2][4] = {};
+        // Aqk on tf32 (m16n8k8), Akk on bf16 (m16n8k16). Within each 16-channel
+        // step the tf32 k slots are permuted (slot q <-> channel 2q, slot q+4 <->
+        // channel 2q+1, for each half) so that one 8-byte load of the scaled
+        // k row feeds both the tf32 and the bf16 B fragments.
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-            uint32_t fa[4], fl[4], fk[4];
-            ldsm_x4(fa, sQ + (16 * i + (lane & 15)) * RSB + 16 * kk + ((lane >> 4) << 3));
-            ldsm_x4(fl, sQlo + (16 * i + (lane & 15)) * RSB + 16 * kk + ((lane >> 4) << 3));
-            ldsm_x4(fk, sK + (16 * i + (lane & 15)) * RSB + 16 * kk + ((lane >> 4) << 3));
             const int c0 = 16 * kk + 2 * qd;
+            uint32_t fa0[4], fa1[4], fk[4];
+            {
+                const uint2 u00 = *reinterpret_cast<const uint2 *>(sQ + qa_pair(16 * i + gq, c0));
+                const uint2 u10 = *reinterpret_cast<const uint2 *>(sQ + qa_pair(16 * i + gq + 8, c0));
+                const uint2 u01 = *reinterpret_cast<const uint2 *>(sQ + qa_pair(16 * i + gq, c0 + 8));
+                const uint2 u11 = *reinterpret_cast<const uint2 *>(sQ + qa_pair(16 * i + gq + 8, c0 + 8));
+                fa0[0] = u00.x; fa0[1] = u10.x; fa0[2] = u00.y; fa0[3] = u10.y;
+                fa1[0] = u01.x; fa1[1] = u11.x; fa1[2] = u01.y; fa1[3] = u11.y;
+            }
+            ldsm_x4(fk, sK + a_addr(lane, 64, 16 * i, 16 * kk));
             float2 f0 = make_float2(1.f, 1.f), f1 = make_float2(1.f, 1.f);
             if (i > j) {
                 f0 = *reinterpret_cast<const float2 *>(fr + c0);
@@ -440,13 +608,10 @@ __device__ __forceinline__ void run_task(const Params &p, unsigned char *smem, u
                 const float *row = nt ? kbrow1 : kbrow0;
                 const float2 x0 = *reinterpret_cast<const float2 *>(row + c0);
                 const float2 x1 = *reinterpret_cast<const float2 *>(row + c0 + 8);
-                uint32_t bh0, bl0, bh1, bl1;
-                split_bf16(x0.x * f0.x, x0.y * f0.y, bh0, bl0);
-                split_bf16(x1.x * f1.x, x1.y * f1.y, bh1, bl1);
-                mma16816(aq[nt], fa, bh0, bh1);
-                mma16816(aq[nt], fl, bh0, bh1);
-                mma16816(aq[nt], fa, bl0, bl1);
-                mma16816(ak[nt], fk, bh0, bh1);
+                const float b00 = x0.x * f0.x, b01 = x0.y * f0.y, b10 = x1.x * f1.x, b11 = x1.y * f1.y;
+                mma1688_tf32(aq[nt], fa0, to_tf32(b00), to_tf32(b01));
+                mma1688_tf32(aq[nt], fa1, to_tf32(b10), to_tf32(b11));
+                mma16816(ak[nt], fk, pack_bf16(b00, b01), pack_bf16(b10, b11));
             }
         }
 #pragma unroll
@@ -465,154 +630,212 @@ __device__ __forceinline__ void run_task(const Params &p, unsigned char *smem, u
                     vk[e] = strict ? bt * ak[nt][2 * hf + e] : 0.f;
                     if (i == j) sLD[(i * 16 + tl) * 17 + sl + e] = vk[e];
                 }
-                *reinterpret_cast<uint32_t *>(sAqk + t * RSA + s) = pack_f16(vq[0], vq[1]);
+                *reinterpret_cast<uint32_t *>(img + SL_AQK + tile_elem(64, t, s)) = pack_f16(vq[0], vq[1]);
                 *reinterpret_cast<uint32_t *>(sL + t * RSA + s) = pack_f16(vk[0], vk[1]);
             }
+        if (i == j) {  // L_ii is in place: hand it to warp 10 + i
+            __syncwarp();
+            named_bar_arrive(2 + i, 64);
+        }
+        if (lane == 0) KDA_TRACE_ANY(p, 40 + warp, 0);
     }
-    // upper tiles of scale*Aqk are zero (the consumer reads the full 64x64)
-    for (int idx = tid; idx < 6 * 16 * 8; idx += NCOMP) {
-        const int tile = idx >> 7, rr = (idx >> 3) & 15, cc = (idx & 7) << 1;
-        const int i = tile < 3 ? 0 : (tile < 5 ? 1 : 2);
-        const int j = tile < 3 ? tile + 1 : (tile < 5 ? tile - 1 : 3);
-        *reinterpret_cast<uint32_t *>(sAqk + (16 * i + rr) * RSA + 16 * j + cc) = 0u;
+    // ---- step 3a, on warps 10-13 while the strips run: T_ii = (I + L_ii)^-1
+    // by fp32 forward substitution, once warp i(i+3)/2 has written L_ii
+    if (warp >= 10 && warp < 14) {
+        const int i = warp - 10;
+        named_bar_sync(2 + i, 64);
+        if (lane < 16) {
+            const int jc = lane;
+            const float *Ld = sLD + i * 16 * 17;
+            float x[16];
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+                float s = (r == jc) ? 1.f : 0.f;
+#pragma unroll
+                for (int cc = 0; cc < r; ++cc) s -= Ld[r * 17 + cc] * x[cc];
+                x[r] = s;
+            }
+#pragma unroll
+            for (int r = 0; r < 16; ++r) sT[(16 * i + r) * RSA + 16 * i + jc] = __float2half_rn(x[r]);
+        }
+        if (lane == 0) KDA_TRACE_ANY(p, 50 + i, 0);
     }
-    sync_compute();
-    // q, k, q*a lo, kb and beta are free: stream in the rest of the next task
-    if (nxt.valid) issue_loads(p, smem, nxt, 1, qlobuf);
+    sync_compute();  // the strips only read the input tiles: their values are in registers by now
+    nxt2 = get_task(misc + 2);
+    const bool slot_ok = misc[9] != 0;
+    // q, k, v, q*a lo, kb and beta are free: stream in the next task
+    if (nxt.valid) {
+        issue_loads(p, smem, nxt, bar_g, bar_q);
+        ++issued;
+    }
+    if (!slot_ok) return false;
     KDA_TRACE_EV(p, 23, 0);
 
-    // ---- step 3a: (I + L_ii)^-1 for the four diagonal blocks, fp32 substitution
-    if (warp < 4 && lane < 16) {
-        const int i = warp, jc = lane;
-        const float *Ld = sLD + i * 16 * 17;
-        float x[16];
-#pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            float s = (r == jc) ? 1.f : 0.f;
-#pragma unroll
-            for (int cc = 0; cc < r; ++cc) s -= Ld[r * 17 + cc] * x[cc];
-            x[r] = s;
-        }
-#pragma unroll
-        for (int r = 0; r < 16; ++r) sInv[(i * 16 + r) * RSI + jc] = __float2half_rn(x[r]);
-    }
-    sync_compute();
-    KDA_TRACE_EV(p, 24, 0);
-
-    // ---- steps 3b/4: X = (I+L)^-1 [beta v | beta k e^G], in place; warp w owns 16 columns
-    {
-        __half *R = (warp < 8) ? sRV : sRK;
-        const int col0 = 16 * (warp & 7);
-        for (int i = 0; i < 4; ++i) {
-            float acc[2][4] = {};
-            for (int j = 0; j < i; ++j) {
+    // ---- step 3b: the blocks of T = (I + L)^-1 below its diagonal, one block
+    // diagonal at a time: T_ij = -T_ii * sum_{k=j}^{i-1} L_ik T_kj
+    for (int d = 1; d < 4; ++d) {
+        if (warp < 4 - d) {
+            const int j = warp, i = warp + d;
+            float m[2][4] = {};
+            for (int kb = j; kb < i; ++kb) {
                 uint32_t fa[4], fb[4];
-                ldsm_x4(fa, sL + (16 * i + (lane & 15)) * RSA + 16 * j + ((lane >> 4) << 3));
-                ldsm_x4_t(fb, R + bk_off(lane, 16 * j, col0, RSB));
-                mma16816_f16(acc[0], fa, fb[0], fb[1]);
-                mma16816_f16(acc[1], fa, fb[2], fb[3]);
+                ldsm_x4(fa, sL + (16 * i + (lane & 15)) * RSA + 16 * kb + ((lane >> 4) << 3));
+                ldsm_x4_t(fb, sT + bk_off(lane, 16 * kb, 16 * j, RSA));
+                mma16816_f16(m[0], fa, fb[0], fb[1]);
+                mma16816_f16(m[1], fa, fb[2], fb[3]);
             }
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    uint32_t *pp = reinterpret_cast<uint32_t *>(R + (16 * i + gq + 8 * hf) * RSB + col0 + 8 * nt + 2 * qd);
-                    const float2 rv = unpack_f16(*pp);
-                    const float y0 = rv.x - acc[nt][2 * hf], y1 = rv.y - acc[nt][2 * hf + 1];
-                    range_bad |= !(f16_ok(y0) && f16_ok(y1));
-                    *pp = pack_f16(y0, y1);
-                }
+                for (int hf = 0; hf < 2; ++hf)
+                    *reinterpret_cast<uint32_t *>(sT + (16 * i + gq + 8 * hf) * RSA + 16 * j + 8 * nt + 2 * qd) =
+                        pack_f16(m[nt][2 * hf], m[nt][2 * hf + 1]);
             __syncwarp();
-            float xo[2][4] = {};
+            float t[2][4] = {};
             {
                 uint32_t fa[4], fb[4];
-                ldsm_x4(fa, sInv + (16 * i + (lane & 15)) * RSI + ((lane >> 4) << 3));
-                ldsm_x4_t(fb, R + bk_off(lane, 16 * i, col0, RSB));
-                mma16816_f16(xo[0], fa, fb[0], fb[1]);
-                mma16816_f16(xo[1], fa, fb[2], fb[3]);
+                ldsm_x4(fa, sT + (16 * i + (lane & 15)) * RSA + 16 * i + ((lane >> 4) << 3));
+                ldsm_x4_t(fb, sT + bk_off(lane, 16 * i, 16 * j, RSA));
+                mma16816_f16(t[0], fa, fb[0], fb[1]);
+                mma16816_f16(t[1], fa, fb[2], fb[3]);
             }
             __syncwarp();
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf)
+                    *reinterpret_cast<uint32_t *>(sT + (16 * i + gq + 8 * hf) * RSA + 16 * j + 8 * nt + 2 * qd) =
+                        pack_f16(-t[nt][2 * hf], -t[nt][2 * hf + 1]);
+        }
+        sync_compute();
+    }
+    KDA_TRACE_EV(p, 24, 0);
+
+    // ---- step 4: [u | w] = T [beta v | beta k e^G], in place in the slot image
+    // (u in U, w in rows 64-127 of A1); warp w owns 16 columns and reads all
+    // four row blocks of them before it writes any
+    {
+        const bool isw = warp >= 8;
+        const int col0 = 16 * (warp & 7);
+        uint32_t rb[4][4];
+#pragma unroll
+        for (int kb = 0; kb < 4; ++kb) ldsm_x4_t(rb[kb], img + uw_bk(isw, lane, 16 * kb, col0));
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float acc[2][4] = {};
+#pragma unroll
+            for (int kb = 0; kb <= i; ++kb) {
+                uint32_t fa[4];
+                ldsm_x4(fa, sT + (16 * i + (lane & 15)) * RSA + 16 * kb + ((lane >> 4) << 3));
+                mma16816_f16(acc[0], fa, rb[kb][0], rb[kb][1]);
+                mma16816_f16(acc[1], fa, rb[kb][2], rb[kb][3]);
+            }
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
                     const int rr = 16 * i + gq + 8 * hf, cc = col0 + 8 * nt + 2 * qd;
-                    range_bad |= !(f16_ok(xo[nt][2 * hf]) && f16_ok(xo[nt][2 * hf + 1]));
-                    *reinterpret_cast<uint32_t *>(R + rr * RSB + cc) = pack_f16(xo[nt][2 * hf], xo[nt][2 * hf + 1]);
+                    range_bad |= !(f16_ok(acc[nt][2 * hf]) && f16_ok(acc[nt][2 * hf + 1]));
+                    *reinterpret_cast<uint32_t *>(img + uw_elem(isw, rr, cc)) = pack_f16(acc[nt][2 * hf], acc[nt][2 * hf + 1]);
                 }
-            __syncwarp();
         }
     }
+    fence_proxy_async_shared();  // this thread's image writes, before the bulk store reads them
     sync_compute();
     KDA_TRACE_EV(p, 25, 0);
 
-    // ---- hand-off: Aqk, u, w and e^(G_last) into the slot (16-byte stores)
-    for (int idx = tid; idx < BT * 8; idx += NCOMP) {
-        const int r = idx >> 3, c8 = (idx & 7) << 3;
-        *reinterpret_cast<uint4 *>(slot + SL_AQK + tile_chunk(64, r, c8)) =
-            *reinterpret_cast<const uint4 *>(sAqk + r * RSA + c8);
-    }
-    for (int idx = tid; idx < BT * 16; idx += NCOMP) {
-        const int r = idx >> 4, c8 = (idx & 15) << 3;
-        *reinterpret_cast<uint4 *>(slot + SL_U + tile_chunk(64, r, c8)) =
-            *reinterpret_cast<const uint4 *>(sRV + r * RSB + c8);
-        *reinterpret_cast<uint4 *>(slot + SL_A1 + tile_chunk(128, 64 + r, c8)) =
-            *reinterpret_cast<const uint4 *>(sRK + r * RSB + c8);
-    }
-    if (tid < 32)
-        *reinterpret_cast<float4 *>(slot + SL_D + 16 * tid) = *reinterpret_cast<const float4 *>(sTab + TD + 4 * tid);
+    // ---- hand-off: the rest of the image (published by REL_TID during the
+    // next task's strips, or after the last task)
+    if (tid == REL_TID) store_late(dst, img);
+    return true;
 }
 
 __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int pid) {
     const int tid = threadIdx.x;
     Ring R = ring_of(p);
     int *misc = reinterpret_cast<int *>(smem + OFF_MISC);
+    // sequence bounds in shared memory (the ring's acquire loads invalidate L1,
+    // so global reads of them would go to L2 on every task)
+    const int32_t *cu_s = p.cu;
+    if (p.N + 1 <= CU_CACHE) {
+        int32_t *c = reinterpret_cast<int32_t *>(smem + OFF_CU);
+        for (int i = tid; i <= p.N; i += NCOMP) c[i] = p.cu[i];
+        cu_s = c;
+    }
     // longest consumer sequence: tasks beyond it do not exist
     if (tid == 0) misc[1] = 0;
     sync_compute();
     {
         int mx = 0;
-        for (int k = tid; k < p.C; k += NCOMP) mx = max(mx, consumer_total(p, k));
+        for (int k = tid; k < p.C; k += NCOMP) mx = max(mx, consumer_total(p, cu_s, k));
         atomicMax(&misc[1], mx);
+    }
+    // the upper 16x16 tiles of scale*Aqk are never written: zero them once
+    for (int idx = tid; idx < 6 * 16 * 8; idx += NCOMP) {
+        const int tile = idx >> 7, rr = (idx >> 3) & 15, cc = (idx & 7) << 1;
+        const int i = tile < 3 ? 0 : (tile < 5 ? 1 : 2);
+        const int j = tile < 3 ? tile + 1 : (tile < 5 ? tile - 1 : 3);
+        *reinterpret_cast<uint32_t *>(smem + OFF_IMG + SL_AQK + tile_elem(64, 16 * i + rr, 16 * j + cc)) = 0u;
+    }
+    uint64_t *bar_g = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
+    uint64_t *bar_q = bar_g + 1;
+    if (tid == 0) {
+        mbar_init(bar_g, 1);
+        mbar_init(bar_q, 1);
+        mbar_fence_init();
     }
     sync_compute();
     const int jmax = misc[1];
-    auto fetch = [&]() {  // all threads; thread 0 draws, everyone reads after the barrier
-        if (tid == 0) {
-            const Task t = fetch_task(p, R, jmax);
-            misc[2] = t.valid; misc[3] = t.k; misc[4] = t.j; misc[5] = t.ch; misc[6] = t.c;
-        }
-        sync_compute();
-        const Task t{misc[2], misc[3], misc[4], misc[5], misc[6]};
-        sync_compute();
-        return t;
-    };
-    Task cur = fetch();
-    int vbuf = OFF_V, qlobuf = OFF_QLO;
+    Cursor cs = make_cursor(pid, static_cast<int>(gridDim.x) - p.C, p.C);  // used by SYNC_TID
+    if (tid == SYNC_TID) {
+        const Task t = fetch_task(p, cu_s, jmax, cs);
+        put_task(misc + 2, t);
+        const Task u = fetch_task(p, cu_s, jmax, cs);
+        put_task(misc + 10, u);
+    }
+    sync_compute();
+    Task cur = get_task(misc + 2);
+    Task nxt = get_task(misc + 10);
+    sync_compute();
+    int issued = 0, landed_g = 0, landed_q = 0;  // load phases, the same in every thread
     if (cur.valid) {
-        issue_loads(p, smem, cur, 0, vbuf);
-        issue_loads(p, smem, cur, 1, vbuf);
+        issue_loads(p, smem, cur, bar_g, bar_q);
+        ++issued;
     }
     bool gate_bad = false, range_bad = false;
+    int pending = -1, pending_val = 0;  // REL_TID: the last slot stored but not yet published
     while (cur.valid) {
-        const Task nxt = fetch();
-        const int s = cur.j % RING;
         KDA_TRACE_EV(p, 1, cur.j * p.C + cur.k);
-        if (tid == 0)
-            misc[7] = (cur.j < RING) ? 1 : (wait_flag_geq(R, &R.freed[cur.k * RING + s], cur.j - RING + 1, p.status) ? 1 : 0);
+        const uint32_t ph = static_cast<uint32_t>(landed_g) & 1u;
         cp_async_wait_all();
+        bool ok = wait_mbar(R, bar_g, ph, p.status);
+        if (cur.nv < BT) ok = ok && wait_mbar(R, bar_q, ph, p.status);  // a tail's rows are zeroed after both
+        if (__syncthreads_or(!ok)) break;  // one decision for the whole CTA
+        ++landed_g;
+        if (cur.nv < BT) zero_tail(smem, cur);
         sync_compute();
-        if (!misc[7]) break;
         KDA_TRACE_EV(p, 20, 0);
-        unsigned char *slot = R.slots + static_cast<size_t>(cur.k * RING + s) * SLOT_BYTES;
-        run_task(p, smem, slot, cur.ch, cur.c, vbuf, qlobuf, nxt, gate_bad, range_bad);
-        sync_compute();  // every thread's slot stores precede the barrier, hence the release below
-        if (tid == 0) st_release(&R.ready[cur.k * RING + s], cur.j + 1);
+        Task nxt2{0, 0, 0, 0, 0, 0, 0};
+        if (!run_task(p, R, smem, cur, cu_s, jmax, nxt, nxt2, cs, pending, pending_val, bar_g, bar_q, ph, landed_q, issued,
+                      gate_bad, range_bad))
+            break;
+        if (tid == REL_TID) {
+            pending = cur.k * RING + cur.j % RING;
+            pending_val = cur.j + 1;
+        }
         KDA_TRACE_EV(p, 3, cur.j * p.C + cur.k);
         cur = nxt;
-        const int tmp = vbuf;
-        vbuf = qlobuf;
-        qlobuf = tmp;
+        nxt = nxt2;
+    }
+    // after an abort: let this CTA's own tensor copies land before it leaves
+    for (; landed_g < issued; ++landed_g) drain_mbar(bar_g, static_cast<uint32_t>(landed_g) & 1u);
+    for (; landed_q < issued; ++landed_q) drain_mbar(bar_q, static_cast<uint32_t>(landed_q) & 1u);
+    if (tid == REL_TID) {
+        bulk_wait_all();
+        if (pending >= 0) {
+            fence_proxy_async_global();
+            st_release(&R.ready[pending], pending_val);
+        }
     }
     cp_async_wait_all();
     if (gate_bad) set_status(p.status, KDA_ERR_GATE_RANGE);
@@ -685,7 +908,7 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
     const uint32_t tmem = *tslot;
     const uint32_t tS = tmem + (static_cast<uint32_t>(32 * quad) << 16) + 32 * slice;  // this thread's S columns
     const uint32_t tD = tS + 128;                                                       // this thread's D columns
-    const int total = consumer_total(p, k);
+    const int total = consumer_total(p, p.cu, k);
 
     auto issue = [&](int jj) {  // slot jj -> buffer jj % 2 (thread 0)
         const unsigned char *src = R.slots + static_cast<size_t>(k * RING + jj % RING) * SLOT_BYTES;
@@ -711,7 +934,7 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
     bool range_bad = false, alive = true;
     for (int ch = k; ch < p.N * p.H && alive; ch += p.C) {
         int64_t bos, len;
-        const int nc = chain_info(p, ch, bos, len);
+        const int nc = chain_info(p, p.cu, ch, bos, len);
         if (nc < 0) {
             if (tid == 0) set_status(p.status, KDA_ERR_BAD_SEQLENS);
             continue;
@@ -922,12 +1145,22 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
 }
 }  // namespace cons
 
-constexpr int SMEM_MAX = (prod::SMEM > cons::SMEM ? prod::SMEM : cons::SMEM) + 1024;  // + alignment slack
+constexpr int SMEM_TILES = (prod::SMEM > cons::SMEM ? prod::SMEM : cons::SMEM) + 1024;  // + alignment slack
+#ifdef KDA_TRACE
+static_assert(SMEM_TILES <= TRACE_COUNTS_OFFSET, "trace counters past the tiles");
+constexpr int SMEM_MAX = TRACE_COUNTS_OFFSET + 64;
+#else
+constexpr int SMEM_MAX = SMEM_TILES;
+#endif
 static_assert(SMEM_MAX <= 232448, "shared memory budget");
 
-__global__ void __launch_bounds__(NTHREADS, 1) kda_persistent_kernel(const Params p) {
+__global__ void __launch_bounds__(NTHREADS, 1) kda_persistent_kernel(const __grid_constant__ Params p) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+#ifdef KDA_TRACE
+    if (threadIdx.x < 16) reinterpret_cast<int *>(smem_raw + TRACE_COUNTS_OFFSET)[threadIdx.x] = 0;
+    __syncthreads();
+#endif
     if (static_cast<int>(blockIdx.x) < p.C)
         cons::run(p, smem, blockIdx.x);
     else
@@ -935,6 +1168,36 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_persistent_kernel(const Param
 }
 
 // ------------------------------------------------------------------ host side
+// cuTensorMapEncodeTiled, looked up once through the runtime (no link-time
+// dependence on the driver library)
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+// [T][H][128] tensor, box = `box_c` channels x 1 head x 64 tokens, 128-byte swizzle
+static bool encode_input_map(CUtensorMap *m, const void *base, bool fp32, int64_t T, int32_t H, uint32_t box_c) {
+    const PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t esz = fp32 ? 4 : 2;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(DK), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(T)};
+    const cuuint64_t strides[2] = {DK * esz, static_cast<cuuint64_t>(H) * DK * esz};
+    const cuuint32_t box[3] = {box_c, 1, static_cast<cuuint32_t>(BT)};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base),
+              dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 static int num_sms() {
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -955,7 +1218,7 @@ size_t workspace_bytes(int64_t chains) {
     const int C = consumers_for(chains, sms);
     size_t bytes = ring_offset(C) + static_cast<size_t>(C) * RING * SLOT_BYTES;
 #ifdef KDA_TRACE
-    bytes += static_cast<size_t>(sms) * (TRACE_EVENTS * 2 + 1) * 8;
+    bytes += static_cast<size_t>(sms) * TRACE_CTA_WORDS * 8;
 #endif
     return bytes;
 }
@@ -971,12 +1234,18 @@ cudaError_t launch(Params p, size_t ws_bytes, cudaStream_t stream) {
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     const int grid = sms;  // one CTA per SM; all co-resident (cooperative launch)
     p.C = consumers_for(static_cast<int64_t>(p.N) * p.H, grid);
+    memset(&p.tm_q, 0, sizeof(CUtensorMap) * 4);
+    if (p.T > 0) {  // with no tokens there are no producer tasks and no loads
+        if (!encode_input_map(&p.tm_q, p.q, false, p.T, p.H, 64) || !encode_input_map(&p.tm_k, p.k, false, p.T, p.H, 64) ||
+            !encode_input_map(&p.tm_v, p.v, false, p.T, p.H, 64) || !encode_input_map(&p.tm_g, p.g, true, p.T, p.H, 32))
+            return cudaErrorInvalidValue;
+    }
     if (ws_bytes < ring_offset(p.C) + static_cast<size_t>(p.C) * RING * SLOT_BYTES) return cudaErrorInvalidValue;
     e = cudaMemsetAsync(p.ws, 0, ring_offset(p.C), stream);
     if (e != cudaSuccess) return e;
 #ifdef KDA_TRACE
     e = cudaMemsetAsync(p.ws + ring_offset(p.C) + static_cast<size_t>(p.C) * RING * SLOT_BYTES, 0,
-                        static_cast<size_t>(grid) * (TRACE_EVENTS * 2 + 1) * 8, stream);
+                        static_cast<size_t>(grid) * TRACE_CTA_WORDS * 8, stream);
     if (e != cudaSuccess) return e;
 #endif
     void *args[] = {&p};
