@@ -240,8 +240,12 @@ constexpr int OFF_BAR = OFF_MISC + 128;       // input-load mbarriers: g, then q
 constexpr int OFF_CU = OFF_BAR + 16;          // copy of cu_seqlens when it has at most CU_CACHE entries
 constexpr int CU_CACHE = 1024;
 constexpr int SMEM = OFF_CU + 4 * CU_CACHE;
-constexpr int SYNC_TID = NCOMP - 32;          // lane 0 of warp 15: draws tasks, waits for free slots
-constexpr int REL_TID = NCOMP - 64;           // lane 0 of warp 14: stores slot images and publishes them
+// Warp w runs on sub-partition w % 4. During the strips, warps 0-9 hold the
+// ten tiles (three on partitions 0 and 1, two on 2 and 3); the diagonal
+// inverses run on warps 10, 11, 14, 15 (partitions 2 and 3) and the ring work,
+// mostly waiting, on warps 12 and 13 (partitions 0 and 1).
+constexpr int SYNC_TID = 13 * 32;             // lane 0 of warp 13: draws tasks
+constexpr int REL_TID = 12 * 32;              // lane 0 of warp 12: waits for free slots, stores and publishes images
 constexpr int TGM = 0, TGL = 4 * 128, TEM = 5 * 128, TEL = 9 * 128, TF = 13 * 128, TD = 19 * 128;
 static_assert(OFF_Q % 1024 == 0 && OFF_GKB % 1024 == 0, "tensor-copy destinations are 1024-byte aligned");
 // byte offset of the 16-byte chunk holding channels [c4, c4+4) of row r of the g tile
@@ -282,15 +286,14 @@ __device__ __forceinline__ int uw_bk(bool isw, int lane, int k0, int n0) {  // l
 }
 
 // A task and where its tokens are: t0 = first token of the chunk, nv = its
-// valid rows (computed once when the task is drawn, so that no later step
-// reads the sequence bounds from global memory again).
+// valid rows, h = its head (computed once when the task is drawn).
 struct Task {
-    int valid, k, j, ch, c, t0, nv;
+    int valid, k, j, ch, c, t0, nv, h;
 };
 __device__ __forceinline__ void put_task(int *m, const Task &t) {
-    m[0] = t.valid; m[1] = t.k; m[2] = t.j; m[3] = t.ch; m[4] = t.c; m[5] = t.t0; m[6] = t.nv;
+    m[0] = t.valid; m[1] = t.k; m[2] = t.j; m[3] = t.ch; m[4] = t.c; m[5] = t.t0; m[6] = t.nv; m[7] = t.h;
 }
-__device__ __forceinline__ Task get_task(const int *m) { return Task{m[0], m[1], m[2], m[3], m[4], m[5], m[6]}; }
+__device__ __forceinline__ Task get_task(const int *m) { return Task{m[0], m[1], m[2], m[3], m[4], m[5], m[6], m[7]}; }
 
 // Tasks are numbered j * C + k (chunk j of consumer k), so every consumer
 // advances together; producer pid takes the numbers pid, pid + P, pid + 2P,
@@ -303,7 +306,7 @@ __device__ __forceinline__ Cursor make_cursor(int pid, int P, int C) { return Cu
 
 // next valid task of the cursor (numbers whose consumer has fewer chunks are skipped)
 __device__ __forceinline__ Task fetch_task(const Params &p, const int32_t *cu, int jmax, Cursor &cs) {
-    Task t{0, 0, 0, 0, 0, 0, 0};
+    Task t{0, 0, 0, 0, 0, 0, 0, 0};
     while (cs.j < jmax) {
         t.k = cs.k;
         t.j = cs.j;
@@ -318,6 +321,7 @@ __device__ __forceinline__ Task fetch_task(const Params &p, const int32_t *cu, i
             const int64_t t0 = bos + static_cast<int64_t>(t.c) * BT;
             t.t0 = static_cast<int>(t0);
             t.nv = static_cast<int>((bos + len - t0) < BT ? (bos + len - t0) : BT);
+            t.h = t.ch % p.H;
             t.valid = 1;
             return t;
         }
@@ -328,12 +332,13 @@ __device__ __forceinline__ Task fetch_task(const Params &p, const int32_t *cu, i
 // One task's inputs into shared memory, called by all threads once the
 // buffers are free: q, k, v and g as ten tiled tensor copies issued by
 // SYNC_TID, g completing on `bar_g` and q, k, v on `bar_q` (one phase per
-// task each, so the prefix sum can start before q, k, v land), beta by cp.async.
+// task each, so the prefix sum can start before q, k, v land), beta by
+// cp.async from warps 14 and 15.
 // Rows past the sequence end are zeroed once the copies have landed.
 __device__ __forceinline__ void issue_loads(const Params &p, unsigned char *smem, const Task &tk, uint64_t *bar_g,
                                             uint64_t *bar_q) {
     const int tid = threadIdx.x;
-    const int h = tk.ch % p.H;
+    const int h = tk.h;
     const int64_t t0 = tk.t0;
     const int nv = tk.nv;
     if (tid == SYNC_TID) {
@@ -348,11 +353,12 @@ __device__ __forceinline__ void issue_loads(const Params &p, unsigned char *smem
         }
         KDA_TRACE_ANY(p, 30, 0);
     }
-    if (tid < BT) {
-        const bool ok = tid < nv;
-        cp_async4(smem + OFF_BETA + 4 * tid, p.beta + static_cast<size_t>(t0 + (ok ? tid : 0)) * p.H + h, ok ? 4 : 0);
+    if (tid >= NCOMP - BT) {  // warps 14 and 15: off the critical path after the strips
+        const int r = tid - (NCOMP - BT);
+        const bool ok = r < nv;
+        cp_async4(smem + OFF_BETA + 4 * r, p.beta + static_cast<size_t>(t0 + (ok ? r : 0)) * p.H + h, ok ? 4 : 0);
+        cp_async_commit();
     }
-    cp_async_commit();
 }
 
 // rows >= nv of the input tiles (the tensor copies read the next sequence
@@ -545,7 +551,7 @@ __device__ __forceinline__ bool run_task(const Params &p, const Ring &Rg, unsign
     sync_compute();
     KDA_TRACE_EV(p, 22, 0);
 
-    // ---- ring work, on warps 14 and 15 (no strip pair, no diagonal block).
+    // ---- ring work, on warps 12 and 13 (no strip pair, no diagonal block).
     // REL_TID: publish the previous slot, then wait for this task's slot and
     // send the part of the image that is final already. SYNC_TID: draw.
     unsigned char *dst = Rg.slots + static_cast<size_t>(cur.k * RING + cur.j % RING) * SLOT_BYTES;
@@ -560,7 +566,7 @@ __device__ __forceinline__ bool run_task(const Params &p, const Ring &Rg, unsign
         const int s = cur.j % RING;
         const bool free_ok =
             (cur.j < RING) || wait_flag_geq(Rg, &Rg.freed[cur.k * RING + s], cur.j - RING + 1, p.status);
-        misc[9] = free_ok ? 1 : 0;
+        misc[20] = free_ok ? 1 : 0;
         if (free_ok) store_early(dst, img);
         KDA_TRACE_ANY(p, 33, 0);
     }
@@ -572,8 +578,12 @@ __device__ __forceinline__ bool run_task(const Params &p, const Ring &Rg, unsign
     // ---- step 2b: Aqk (tf32) and Akk (bf16) on the 10
     // lower 16x16 tiles, one tile per warp. Tile (i,j) needs k_s e^(G_{m_i} - G_s)
     // for s in sub-block j: the stored k e^(G_{m_j} - G) times e^(G_{m_i} - G_{m_j}) (<= 1).
-    static_assert(NWARPS == 16, "warps 0-9 strips, 10-13 diagonal inverses, 14-15 ring work");
-    for (int pair = warp; pair < 10; pair += NWARPS) {
+    static_assert(NWARPS == 16, "warps 0-9 strips, 10, 11, 14, 15 diagonal inverses, 12-13 ring work");
+    // Warp w runs on sub-partition w % 4, so warps 0-9 leave partitions 0 and 1
+    // with three tiles and 2 and 3 with two: the diagonal tiles (pairs 0, 2, 5,
+    // 9), whose L_ii feed the inverses, go to warps 2, 3, 6, 7 on the lighter ones.
+    if (warp < 10) {
+        const int pair = (0x8795642031ull >> (4 * warp)) & 15;  // warp -> pair: 1 3 0 2 4 6 5 9 7 8
         int i = 0;
         while ((i + 1) * (i + 2) / 2 <= pair) ++i;
         const int j = pair - i * (i + 1) / 2;
@@ -633,16 +643,17 @@ __device__ __forceinline__ bool run_task(const Params &p, const Ring &Rg, unsign
                 *reinterpret_cast<uint32_t *>(img + SL_AQK + tile_elem(64, t, s)) = pack_f16(vq[0], vq[1]);
                 *reinterpret_cast<uint32_t *>(sL + t * RSA + s) = pack_f16(vk[0], vk[1]);
             }
-        if (i == j) {  // L_ii is in place: hand it to warp 10 + i
+        if (i == j) {  // L_ii is in place: hand it to the inverse warp of block i
             __syncwarp();
             named_bar_arrive(2 + i, 64);
         }
         if (lane == 0) KDA_TRACE_ANY(p, 40 + warp, 0);
     }
-    // ---- step 3a, on warps 10-13 while the strips run: T_ii = (I + L_ii)^-1
-    // by fp32 forward substitution, once warp i(i+3)/2 has written L_ii
-    if (warp >= 10 && warp < 14) {
-        const int i = warp - 10;
+    // ---- step 3a, on warps 10, 11, 14, 15 (blocks 0-3) while the strips run:
+    // T_ii = (I + L_ii)^-1 by fp32 forward substitution, once the warp with
+    // tile (i, i) has written L_ii
+    if (warp == 10 || warp == 11 || warp == 14 || warp == 15) {
+        const int i = (warp & 1) | ((warp & 4) >> 1);
         named_bar_sync(2 + i, 64);
         if (lane < 16) {
             const int jc = lane;
@@ -662,7 +673,7 @@ __device__ __forceinline__ bool run_task(const Params &p, const Ring &Rg, unsign
     }
     sync_compute();  // the strips only read the input tiles: their values are in registers by now
     nxt2 = get_task(misc + 2);
-    const bool slot_ok = misc[9] != 0;
+    const bool slot_ok = misc[20] != 0;
     // q, k, v, q*a lo, kb and beta are free: stream in the next task
     if (nxt.valid) {
         issue_loads(p, smem, nxt, bar_g, bar_q);
@@ -671,49 +682,12 @@ __device__ __forceinline__ bool run_task(const Params &p, const Ring &Rg, unsign
     if (!slot_ok) return false;
     KDA_TRACE_EV(p, 23, 0);
 
-    // ---- step 3b: the blocks of T = (I + L)^-1 below its diagonal, one block
-    // diagonal at a time: T_ij = -T_ii * sum_{k=j}^{i-1} L_ik T_kj
-    for (int d = 1; d < 4; ++d) {
-        if (warp < 4 - d) {
-            const int j = warp, i = warp + d;
-            float m[2][4] = {};
-            for (int kb = j; kb < i; ++kb) {
-                uint32_t fa[4], fb[4];
-                ldsm_x4(fa, sL + (16 * i + (lane & 15)) * RSA + 16 * kb + ((lane >> 4) << 3));
-                ldsm_x4_t(fb, sT + bk_off(lane, 16 * kb, 16 * j, RSA));
-                mma16816_f16(m[0], fa, fb[0], fb[1]);
-                mma16816_f16(m[1], fa, fb[2], fb[3]);
-            }
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf)
-                    *reinterpret_cast<uint32_t *>(sT + (16 * i + gq + 8 * hf) * RSA + 16 * j + 8 * nt + 2 * qd) =
-                        pack_f16(m[nt][2 * hf], m[nt][2 * hf + 1]);
-            __syncwarp();
-            float t[2][4] = {};
-            {
-                uint32_t fa[4], fb[4];
-                ldsm_x4(fa, sT + (16 * i + (lane & 15)) * RSA + 16 * i + ((lane >> 4) << 3));
-                ldsm_x4_t(fb, sT + bk_off(lane, 16 * i, 16 * j, RSA));
-                mma16816_f16(t[0], fa, fb[0], fb[1]);
-                mma16816_f16(t[1], fa, fb[2], fb[3]);
-            }
-            __syncwarp();
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf)
-                    *reinterpret_cast<uint32_t *>(sT + (16 * i + gq + 8 * hf) * RSA + 16 * j + 8 * nt + 2 * qd) =
-                        pack_f16(-t[nt][2 * hf], -t[nt][2 * hf + 1]);
-        }
-        sync_compute();
-    }
-    KDA_TRACE_EV(p, 24, 0);
-
-    // ---- step 4: [u | w] = T [beta v | beta k e^G], in place in the slot image
-    // (u in U, w in rows 64-127 of A1); warp w owns 16 columns and reads all
-    // four row blocks of them before it writes any
+    // ---- steps 3b and 4, interleaved. Block row i of X = [u | w] =
+    // T [beta v | beta k e^G] needs block rows 0..i of T = (I + L)^-1 only, so
+    // while all warps compute X_i, warps 0 .. 2-i build block diagonal i+1 of T:
+    // T_ij = -T_ii * sum_{k=j}^{i-1} L_ik T_kj. X is written in place in the
+    // slot image (u in U, w in rows 64-127 of A1); warp w owns 16 columns and
+    // holds all four row blocks of them in registers before it writes any.
     {
         const bool isw = warp >= 8;
         const int col0 = 16 * (warp & 7);
@@ -721,12 +695,46 @@ __device__ __forceinline__ bool run_task(const Params &p, const Ring &Rg, unsign
 #pragma unroll
         for (int kb = 0; kb < 4; ++kb) ldsm_x4_t(rb[kb], img + uw_bk(isw, lane, 16 * kb, col0));
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int xi = 0; xi < 4; ++xi) {
+            const int d = xi + 1;
+            if (d < 4 && warp < 4 - d) {
+                const int j = warp, i = warp + d;
+                float m[2][4] = {};
+                for (int kb = j; kb < i; ++kb) {
+                    uint32_t fa[4], fb[4];
+                    ldsm_x4(fa, sL + (16 * i + (lane & 15)) * RSA + 16 * kb + ((lane >> 4) << 3));
+                    ldsm_x4_t(fb, sT + bk_off(lane, 16 * kb, 16 * j, RSA));
+                    mma16816_f16(m[0], fa, fb[0], fb[1]);
+                    mma16816_f16(m[1], fa, fb[2], fb[3]);
+                }
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf)
+                        *reinterpret_cast<uint32_t *>(sT + (16 * i + gq + 8 * hf) * RSA + 16 * j + 8 * nt + 2 * qd) =
+                            pack_f16(m[nt][2 * hf], m[nt][2 * hf + 1]);
+                __syncwarp();
+                float t[2][4] = {};
+                {
+                    uint32_t fa[4], fb[4];
+                    ldsm_x4(fa, sT + (16 * i + (lane & 15)) * RSA + 16 * i + ((lane >> 4) << 3));
+                    ldsm_x4_t(fb, sT + bk_off(lane, 16 * i, 16 * j, RSA));
+                    mma16816_f16(t[0], fa, fb[0], fb[1]);
+                    mma16816_f16(t[1], fa, fb[2], fb[3]);
+                }
+                __syncwarp();
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf)
+                        *reinterpret_cast<uint32_t *>(sT + (16 * i + gq + 8 * hf) * RSA + 16 * j + 8 * nt + 2 * qd) =
+                            pack_f16(-t[nt][2 * hf], -t[nt][2 * hf + 1]);
+            }
             float acc[2][4] = {};
 #pragma unroll
-            for (int kb = 0; kb <= i; ++kb) {
+            for (int kb = 0; kb <= xi; ++kb) {
                 uint32_t fa[4];
-                ldsm_x4(fa, sT + (16 * i + (lane & 15)) * RSA + 16 * kb + ((lane >> 4) << 3));
+                ldsm_x4(fa, sT + (16 * xi + (lane & 15)) * RSA + 16 * kb + ((lane >> 4) << 3));
                 mma16816_f16(acc[0], fa, rb[kb][0], rb[kb][1]);
                 mma16816_f16(acc[1], fa, rb[kb][2], rb[kb][3]);
             }
@@ -734,12 +742,14 @@ __device__ __forceinline__ bool run_task(const Params &p, const Ring &Rg, unsign
             for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
-                    const int rr = 16 * i + gq + 8 * hf, cc = col0 + 8 * nt + 2 * qd;
+                    const int rr = 16 * xi + gq + 8 * hf, cc = col0 + 8 * nt + 2 * qd;
                     range_bad |= !(f16_ok(acc[nt][2 * hf]) && f16_ok(acc[nt][2 * hf + 1]));
                     *reinterpret_cast<uint32_t *>(img + uw_elem(isw, rr, cc)) = pack_f16(acc[nt][2 * hf], acc[nt][2 * hf + 1]);
                 }
+            if (xi < 3) sync_compute();  // block diagonal d of T is complete
         }
     }
+    KDA_TRACE_EV(p, 24, 0);
     fence_proxy_async_shared();  // this thread's image writes, before the bulk store reads them
     sync_compute();
     KDA_TRACE_EV(p, 25, 0);
@@ -815,7 +825,7 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int pi
         if (cur.nv < BT) zero_tail(smem, cur);
         sync_compute();
         KDA_TRACE_EV(p, 20, 0);
-        Task nxt2{0, 0, 0, 0, 0, 0, 0};
+        Task nxt2{0, 0, 0, 0, 0, 0, 0, 0};
         if (!run_task(p, R, smem, cur, cu_s, jmax, nxt, nxt2, cs, pending, pending_val, bar_g, bar_q, ph, landed_q, issued,
                       gate_bad, range_bad))
             break;
