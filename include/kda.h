@@ -171,6 +171,32 @@ kda_status_t kda_chunk_fwd_static_scratch(const void *q, const void *k, const vo
                                           float *o, float *final_state, int32_t *status_dev,
                                           kda_stream_t stream);
 
+/*
+ * kda_chunk_fwd_debug — kda_chunk_fwd with diagnostic flags, for testing the
+ * failure detection without a GPU fault. Arguments, layouts, ownership and
+ * return codes are those of kda_chunk_fwd; debug_flags is a combination of:
+ *
+ *   KDA_DEBUG_WITHHOLD_READY  producers compute every chunk but never publish
+ *                             it to its consumer, so the consumers' waits for
+ *                             their first chunk run out: the device reports
+ *                             KDA_ERR_TIMEOUT in status_dev, every CTA leaves
+ *                             (after its own copies have landed and its tensor
+ *                             memory is freed) and the context stays usable.
+ *
+ * With any flag set, a wait gives up after 2^14 polls (milliseconds) instead
+ * of 2^24; o and final_state are then unspecified. debug_flags = 0 is exactly
+ * kda_chunk_fwd. Unknown flags return KDA_ERR_INVALID_ARG.
+ * (Not part of the method: the pages define no counterpart.)
+ */
+#define KDA_DEBUG_WITHHOLD_READY 1u
+kda_status_t kda_chunk_fwd_debug(const void *q, const void *k, const void *v, const float *g,
+                                 const float *beta, const int32_t *cu_seqlens, int32_t num_seqs,
+                                 int64_t total_tokens, int32_t num_heads, int32_t head_dim_k,
+                                 int32_t head_dim_v, const float *initial_state, float scale,
+                                 float lower_bound, float *o, float *final_state,
+                                 int32_t *status_dev, void *workspace, size_t workspace_bytes,
+                                 kda_stream_t stream, uint32_t debug_flags);
+
 /* Number of kernel launches one kda_chunk_fwd call makes for these sizes
  * (0 when num_seqs == 0). Host-only, no CUDA call. */
 int32_t kda_chunk_fwd_launches(int32_t num_seqs, int64_t total_tokens, int32_t num_heads);

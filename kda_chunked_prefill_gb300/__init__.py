@@ -5,14 +5,16 @@ The computation lives in hand-written sm_103a CUDA kernels behind a C ABI
 holds the ctypes binding (``_lib``), the build script and the seeded input
 generators (``inputs``).
 """
-from ._lib import (KDA_ERR_BAD_SEQLENS, KDA_ERR_CUDA, KDA_ERR_GATE_RANGE, KDA_ERR_INVALID_ARG,
-                   KDA_ERR_TIMEOUT, KDA_ERR_UNSUPPORTED, KDA_ERR_VALUE_RANGE, KDA_OK, KdaError, chunk_fwd,
+from ._lib import (KDA_DEBUG_WITHHOLD_READY, KDA_ERR_BAD_SEQLENS, KDA_ERR_CUDA, KDA_ERR_GATE_RANGE,
+                   KDA_ERR_INVALID_ARG, KDA_ERR_SCRATCH_TOO_SMALL, KDA_ERR_TIMEOUT, KDA_ERR_UNSUPPORTED,
+                   KDA_ERR_VALUE_RANGE, KDA_OK, KdaError, chunk_fwd,
                    chunk_fwd_launches, kda_chunk_fwd, library_path, load_library, status_string,
                    version, workspace_for, workspace_size)
 
 __all__ = [
     "KDA_OK", "KDA_ERR_INVALID_ARG", "KDA_ERR_UNSUPPORTED", "KDA_ERR_CUDA", "KDA_ERR_GATE_RANGE",
-    "KDA_ERR_BAD_SEQLENS", "KDA_ERR_TIMEOUT", "KDA_ERR_VALUE_RANGE", "KdaError", "chunk_fwd", "chunk_fwd_launches",
+    "KDA_ERR_BAD_SEQLENS", "KDA_ERR_TIMEOUT", "KDA_ERR_VALUE_RANGE", "KDA_ERR_SCRATCH_TOO_SMALL",
+    "KDA_DEBUG_WITHHOLD_READY", "KdaError", "chunk_fwd", "chunk_fwd_launches",
     "kda_chunk_fwd", "library_path", "load_library", "status_string", "version", "workspace_for",
     "workspace_size",
 ]

@@ -25,10 +25,11 @@ KDA_ERR_BAD_SEQLENS = 5
 KDA_ERR_TIMEOUT = 6
 KDA_ERR_VALUE_RANGE = 7
 KDA_ERR_SCRATCH_TOO_SMALL = 8
+KDA_DEBUG_WITHHOLD_READY = 1
 
 HEAD_DIM = 128
-EXPORTED = ("kda_chunk_fwd", "kda_chunk_fwd_workspace_size", "kda_chunk_fwd_launches",
-            "kda_status_string", "kda_version")
+EXPORTED = ("kda_chunk_fwd", "kda_chunk_fwd_workspace_size", "kda_chunk_fwd_static_scratch",
+            "kda_chunk_fwd_debug", "kda_chunk_fwd_launches", "kda_status_string", "kda_version")
 
 _lock = threading.Lock()
 _lib = None
@@ -60,6 +61,8 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.kda_chunk_fwd.argtypes = [vp, vp, vp, vp, vp, vp, i32, i64, i32, i32, i32, vp, f32, f32,
                                       vp, vp, vp, vp, ctypes.c_size_t, vp]
         lib.kda_chunk_fwd.restype = ctypes.c_int
+        lib.kda_chunk_fwd_debug.argtypes = lib.kda_chunk_fwd.argtypes + [ctypes.c_uint32]
+        lib.kda_chunk_fwd_debug.restype = ctypes.c_int
         lib.kda_chunk_fwd_workspace_size.argtypes = [i32, i32]
         lib.kda_chunk_fwd_workspace_size.restype = ctypes.c_size_t
         lib.kda_chunk_fwd_launches.argtypes = [i32, i64, i32]
@@ -120,7 +123,7 @@ def _check(t, name, dtype, shape, device):
 
 
 def kda_chunk_fwd(q, k, v, g, beta, cu_seqlens, initial_state, scale: float, lower_bound: float,
-                  o, final_state, status=None, stream=None, workspace=None) -> int:
+                  o, final_state, status=None, stream=None, workspace=None, debug_flags: int = 0) -> int:
     """Call the C entry point ``kda_chunk_fwd`` with caller-allocated outputs.
 
     q, k, v: bf16 [T,H,128]; o: fp32 [T,H,128]; g: fp32 [T,H,128]; beta: fp32 [T,H];
@@ -129,7 +132,8 @@ def kda_chunk_fwd(q, k, v, g, beta, cu_seqlens, initial_state, scale: float, low
     ``workspace_size(N, H)`` bytes (default: a cached per-device buffer). All on
     one CUDA device. ``stream`` is a ``torch.cuda.Stream`` (default: the current
     stream). Raises ``KdaError`` on a host-side error; returns ``KDA_OK`` once
-    the work is queued.
+    the work is queued. A nonzero ``debug_flags`` calls ``kda_chunk_fwd_debug``
+    (failure-detection testing; see include/kda.h).
     """
     T, H, D = q.shape
     N = cu_seqlens.shape[0] - 1
@@ -155,10 +159,11 @@ def kda_chunk_fwd(q, k, v, g, beta, cu_seqlens, initial_state, scale: float, low
         workspace = workspace_for(N, H, dev)
     if workspace.device != dev or workspace.dtype != torch.uint8 or not workspace.is_contiguous():
         raise ValueError("workspace must be a contiguous uint8 tensor on the inputs' device")
-    rc = load_library().kda_chunk_fwd(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), N, T, H, D, v.shape[2],
-        _ptr(initial_state), float(scale), float(lower_bound), _ptr(o), _ptr(final_state),
-        _ptr(status), _ptr(workspace), workspace.numel(), ctypes.c_void_p(stream.cuda_stream))
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), N, T, H, D, v.shape[2],
+            _ptr(initial_state), float(scale), float(lower_bound), _ptr(o), _ptr(final_state),
+            _ptr(status), _ptr(workspace), workspace.numel(), ctypes.c_void_p(stream.cuda_stream))
+    lib = load_library()
+    rc = lib.kda_chunk_fwd_debug(*args, int(debug_flags)) if debug_flags else lib.kda_chunk_fwd(*args)
     if rc != KDA_OK:
         raise KdaError(rc, "kda_chunk_fwd")
     return rc

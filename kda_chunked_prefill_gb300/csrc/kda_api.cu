@@ -20,15 +20,12 @@ bool lower_bound_ok(float lb) { return lb >= -10.9f && lb <= 0.0f; }
 
 }  // namespace
 
-extern "C" {
-
-kda_status_t kda_chunk_fwd(const void *q, const void *k, const void *v, const float *g,
-                           const float *beta, const int32_t *cu_seqlens, int32_t num_seqs,
-                           int64_t total_tokens, int32_t num_heads, int32_t head_dim_k,
-                           int32_t head_dim_v, const float *initial_state, float scale,
-                           float lower_bound, float *o, float *final_state,
-                           int32_t *status_dev, void *workspace, size_t workspace_bytes,
-                           kda_stream_t stream) {
+namespace {
+kda_status_t fwd_impl(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                      const int32_t *cu_seqlens, int32_t num_seqs, int64_t total_tokens, int32_t num_heads,
+                      int32_t head_dim_k, int32_t head_dim_v, const float *initial_state, float scale,
+                      float lower_bound, float *o, float *final_state, int32_t *status_dev, void *workspace,
+                      size_t workspace_bytes, kda_stream_t stream, uint32_t debug_flags) {
     if (head_dim_k != KDA_HEAD_DIM || head_dim_v != KDA_HEAD_DIM) return KDA_ERR_UNSUPPORTED;
     if (num_seqs < 0 || total_tokens < 0 || num_heads < 1) return KDA_ERR_INVALID_ARG;
     if (static_cast<int64_t>(num_seqs) * num_heads > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
@@ -73,8 +70,38 @@ kda_status_t kda_chunk_fwd(const void *q, const void *k, const void *v, const fl
     p.status = status_dev;
     p.ws = static_cast<unsigned char *>(workspace);
     p.C = 0;
+    p.debug = debug_flags;
+    p.spin = 0;
     const cudaError_t e = kda::pers::launch(p, workspace_bytes, s);
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+}  // namespace
+
+extern "C" {
+
+kda_status_t kda_chunk_fwd(const void *q, const void *k, const void *v, const float *g,
+                           const float *beta, const int32_t *cu_seqlens, int32_t num_seqs,
+                           int64_t total_tokens, int32_t num_heads, int32_t head_dim_k,
+                           int32_t head_dim_v, const float *initial_state, float scale,
+                           float lower_bound, float *o, float *final_state,
+                           int32_t *status_dev, void *workspace, size_t workspace_bytes,
+                           kda_stream_t stream) {
+    return fwd_impl(q, k, v, g, beta, cu_seqlens, num_seqs, total_tokens, num_heads, head_dim_k, head_dim_v,
+                    initial_state, scale, lower_bound, o, final_state, status_dev, workspace, workspace_bytes,
+                    stream, 0u);
+}
+
+kda_status_t kda_chunk_fwd_debug(const void *q, const void *k, const void *v, const float *g,
+                                 const float *beta, const int32_t *cu_seqlens, int32_t num_seqs,
+                                 int64_t total_tokens, int32_t num_heads, int32_t head_dim_k,
+                                 int32_t head_dim_v, const float *initial_state, float scale,
+                                 float lower_bound, float *o, float *final_state,
+                                 int32_t *status_dev, void *workspace, size_t workspace_bytes,
+                                 kda_stream_t stream, uint32_t debug_flags) {
+    if (debug_flags & ~static_cast<uint32_t>(KDA_DEBUG_WITHHOLD_READY)) return KDA_ERR_INVALID_ARG;
+    return fwd_impl(q, k, v, g, beta, cu_seqlens, num_seqs, total_tokens, num_heads, head_dim_k, head_dim_v,
+                    initial_state, scale, lower_bound, o, final_state, status_dev, workspace, workspace_bytes,
+                    stream, debug_flags);
 }
 
 size_t kda_chunk_fwd_workspace_size(int32_t num_seqs, int32_t num_heads) {

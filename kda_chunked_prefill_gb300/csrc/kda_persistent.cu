@@ -35,7 +35,8 @@ namespace pers {
 constexpr int NCOMP = 512;            // 16 warps, all computing (<= 128 registers each)
 constexpr int NTHREADS = NCOMP;
 constexpr int NWARPS = NCOMP / 32;
-constexpr long long SPIN_LIMIT = 1ll << 24;
+constexpr long long SPIN_LIMIT = 1ll << 24;         // polls before a wait gives up (normal calls)
+constexpr long long SPIN_LIMIT_DEBUG = 1ll << 14;   // the same under any KDA_DEBUG_* flag
 #ifdef KDA_TRACE
 constexpr int TRACE_COUNTS_OFFSET = 231424;  // past every role's tiles (checked below), 16 ints
 #endif
@@ -122,6 +123,7 @@ struct Ring {
     int *ready;  // [C][RING]: chunk index + 1 held by the slot
     int *freed;  // [C][RING]: chunk index + 1 the consumer has copied out
     unsigned char *slots;
+    long long spin;  // polls before a wait gives up
 };
 
 __device__ __forceinline__ Ring ring_of(const Params &p) {
@@ -130,11 +132,12 @@ __device__ __forceinline__ Ring ring_of(const Params &p) {
     r.ready = reinterpret_cast<int *>(p.ws + sizeof(Header));
     r.freed = r.ready + p.C * RING;
     r.slots = p.ws + ring_offset(p.C);
+    r.spin = p.spin;
     return r;
 }
 
 __device__ __forceinline__ bool wait_flag_geq(const Ring &R, const int *flag, int target, int32_t *status) {
-    for (long long it = 0; it < SPIN_LIMIT; ++it) {
+    for (long long it = 0; it < R.spin; ++it) {
         if (ld_acquire(flag) >= target) return true;
         if ((it & 127) == 127 && ld_relaxed(&R.hdr->abort)) return false;
         __nanosleep(64);
@@ -145,7 +148,7 @@ __device__ __forceinline__ bool wait_flag_geq(const Ring &R, const int *flag, in
 }
 
 __device__ __forceinline__ bool wait_mbar(const Ring &R, uint64_t *bar, uint32_t parity, int32_t *status) {
-    for (long long it = 0; it < SPIN_LIMIT; ++it) {
+    for (long long it = 0; it < R.spin; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 127) == 127 && ld_relaxed(&R.hdr->abort)) return false;
         __nanosleep(32);
@@ -559,7 +562,7 @@ __device__ __forceinline__ bool run_task(const Params &p, const Ring &Rg, unsign
         if (pending >= 0) {
             bulk_wait_all();
             fence_proxy_async_global();
-            st_release(&Rg.ready[pending], pending_val);
+            if (!(p.debug & KDA_DEBUG_WITHHOLD_READY)) st_release(&Rg.ready[pending], pending_val);
             pending = -1;
         }
         KDA_TRACE_ANY(p, 31, 0);
@@ -844,7 +847,7 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int pi
         bulk_wait_all();
         if (pending >= 0) {
             fence_proxy_async_global();
-            st_release(&R.ready[pending], pending_val);
+            if (!(p.debug & KDA_DEBUG_WITHHOLD_READY)) st_release(&R.ready[pending], pending_val);
         }
     }
     cp_async_wait_all();
@@ -877,10 +880,11 @@ constexpr int OST = 132;                        // fp32 row stride of the o stag
 static_assert(64 * OST * 4 <= 32768 + 16384, "o staging fits in the state and v_new tiles");
 __device__ __forceinline__ bool f16_ok(float x) { return fabsf(x) < F16_SAFE; }
 
+// completion of this CTA's own MMAs: depends on no other CTA, so only a
+// (bounded) timeout ends it early, never the abort word
 __device__ __forceinline__ bool wait_all(const Ring &R, uint64_t *bar, uint32_t parity, int32_t *status) {
     for (long long it = 0; it < SPIN_LIMIT; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 1023) == 1023 && ld_relaxed(&R.hdr->abort)) return false;
     }
     set_status(status, KDA_ERR_TIMEOUT);
     atomicExch(&R.hdr->abort, 1);
@@ -978,7 +982,8 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
             KDA_TRACE_EV(p, 10, j);
             // (1) slot j has landed: release its ring slot, start fetching slot j + 1
             if (tid == 0) {
-                if (misc[0] && wait_mbar(R, &full[b], (j >> 1) & 1, p.status)) {
+                const bool was_alive = misc[0] != 0;  // then slot j's copy has been issued
+                if (was_alive && wait_mbar(R, &full[b], (j >> 1) & 1, p.status)) {
                     fence_proxy_async_global();
                     st_release(&R.freed[k * RING + j % RING], j + 1);
                     issued_next = false;
@@ -987,6 +992,7 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
                         issued_next = true;
                     }
                 } else {
+                    if (was_alive) drain_mbar(&full[b], (j >> 1) & 1);  // let it land before leaving
                     misc[0] = 0;
                 }
             }
@@ -1244,6 +1250,7 @@ cudaError_t launch(Params p, size_t ws_bytes, cudaStream_t stream) {
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     const int grid = sms;  // one CTA per SM; all co-resident (cooperative launch)
     p.C = consumers_for(static_cast<int64_t>(p.N) * p.H, grid);
+    p.spin = p.debug ? SPIN_LIMIT_DEBUG : SPIN_LIMIT;
     memset(&p.tm_q, 0, sizeof(CUtensorMap) * 4);
     if (p.T > 0) {  // with no tokens there are no producer tasks and no loads
         if (!encode_input_map(&p.tm_q, p.q, false, p.T, p.H, 64) || !encode_input_map(&p.tm_k, p.k, false, p.T, p.H, 64) ||

@@ -27,7 +27,9 @@ struct Params {
     float *o, *sT;
     int32_t *status;
     unsigned char *ws;
-    int32_t C;  // consumer CTAs (set by launch)
+    int32_t C;           // consumer CTAs (set by launch)
+    uint32_t debug;      // KDA_DEBUG_* flags (0 in normal calls)
+    long long spin;      // polls before a wait gives up
 };
 
 // workspace: [64-byte header][ready C*RING][freed C*RING] padded to 1024, then the slots

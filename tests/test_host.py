@@ -78,9 +78,34 @@ def _call(lib, **over):
     ({"N": 0, "T": 5}, kda.KDA_ERR_INVALID_ARG),
     ({"ws": None}, kda.KDA_ERR_INVALID_ARG),
     ({"ws": ctypes.c_void_p(0x10008)}, kda.KDA_ERR_INVALID_ARG),
+    ({"T": 2 ** 31}, kda.KDA_ERR_UNSUPPORTED),  # beyond the 32-bit token coordinates
 ])
 def test_host_validation_rejects(lib, over, code):
     assert _call(lib, **over) == code
+
+
+def _call_debug(lib, flags, **over):
+    fake = ctypes.c_void_p(0x10000)
+    args = dict(q=fake, k=fake, v=fake, g=fake, beta=fake, cu=fake, N=2, T=100, H=4, dk=128, dv=128,
+                s0=None, scale=0.088, lb=-5.0, o=fake, sT=None, status=None, ws=fake, wsb=1 << 20,
+                stream=None)
+    args.update(over)
+    return lib.kda_chunk_fwd_debug(args["q"], args["k"], args["v"], args["g"], args["beta"], args["cu"],
+                                   args["N"], args["T"], args["H"], args["dk"], args["dv"], args["s0"],
+                                   args["scale"], args["lb"], args["o"], args["sT"], args["status"],
+                                   args["ws"], args["wsb"], args["stream"], flags)
+
+
+def test_debug_entry_rejects_unknown_flags(lib):
+    assert _call_debug(lib, 2) == kda.KDA_ERR_INVALID_ARG
+    assert _call_debug(lib, 0x80000001) == kda.KDA_ERR_INVALID_ARG
+
+
+def test_debug_entry_validates_like_the_plain_call(lib):
+    assert _call_debug(lib, kda.KDA_DEBUG_WITHHOLD_READY, dk=64) == kda.KDA_ERR_UNSUPPORTED
+    assert _call_debug(lib, kda.KDA_DEBUG_WITHHOLD_READY, q=None) == kda.KDA_ERR_INVALID_ARG
+    assert _call_debug(lib, kda.KDA_DEBUG_WITHHOLD_READY, N=0, T=0, q=None, k=None, v=None, g=None,
+                       beta=None, o=None, cu=None) == kda.KDA_OK
 
 
 def test_workspace_size_is_zero_for_empty_problems(lib):
