@@ -38,6 +38,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "KDA prefill tokens/s at T=8192,H=16,K=V=128 bf16; % of roofline (tensor/HBM)"
+DECODE_METRIC = "KDA decode tokens/s ({n} sequences x {tn} tokens, H={h}, K=V=128, state in/out)"
 UNIT = "tokens/s"
 DEFAULT_WORKLOAD = "headline_4x2048_H16"
 # Context only (another machine): the TPU report's fully optimised headline,
@@ -167,9 +168,12 @@ def max_over_ranks(x: float, world: int) -> float:
     return float(t.item())
 
 
-def source_stamp():
+KERNEL_SOURCES = {"kda_persistent_kernel": "kda_persistent.cu", "kda_decode_kernel": "kda_decode.cu"}
+
+
+def source_stamp(kernel):
     from kda_chunked_prefill_gb300 import build as kbuild
-    return kbuild._stamp()
+    return kbuild.kernel_stamp(KERNEL_SOURCES[kernel])
 
 
 def traffic_from_profile(workload, kernel):
@@ -181,7 +185,7 @@ def traffic_from_profile(workload, kernel):
     try:
         d = json.load(open(p))
         for e in d.get("entries", []):
-            if e.get("workload") == workload and e.get("kernel") == kernel and e.get("source_stamp") == source_stamp():
+            if e.get("workload") == workload and e.get("kernel") == kernel and e.get("source_stamp") == source_stamp(kernel):
                 return float(e["dram_bytes_per_launch"])
     except (ValueError, KeyError, OSError):
         return None
@@ -301,10 +305,15 @@ def bench_gpu(a, world, rank, local):
     fs = torch.empty((N, H, D, D), dtype=torch.float32, device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
+    decode = wl.kind == "decode"
 
     def step():
-        kda.kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], d["initial_state"],
-                          inp["scale"], inp["lower_bound"], o, fs, None, stream)
+        if decode:
+            kda.kda_decode_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], N, d["initial_state"], inp["scale"],
+                               inp["lower_bound"], o, fs, None, stream)
+        else:
+            kda.kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], d["initial_state"],
+                              inp["scale"], inp["lower_bound"], o, fs, None, stream)
 
     for _ in range(max(3, a.warmup)):
         flush.zero_()
@@ -366,9 +375,9 @@ def bench_gpu(a, world, rank, local):
     alg_bytes = algorithmic_bytes(T, N, H, with_init)
     mean_launch_s = (sum(step_ms) / len(step_ms)) / 1e3
     achieved_gbs = alg_bytes / mean_launch_s / 1e9
-    kernel = "kda_persistent_kernel"
+    kernel = "kda_decode_kernel" if decode else "kda_persistent_kernel"
     traffic = traffic_from_profile(a.workload, kernel)
-    flops = algorithmic_flops(inp["seqlens"], H)
+    flops = 0.0 if decode else algorithmic_flops(inp["seqlens"], H)
 
     out = None
     if rank == 0:
@@ -377,10 +386,11 @@ def bench_gpu(a, world, rank, local):
             cpu = cpu_baseline(inp)
         clocks = sampler.summary()
         out = {
-            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": a.steps,
+            "metric": (DECODE_METRIC.format(n=N, tn=T // N, h=H) if decode else METRIC), "value": value, "unit": UNIT, "n_gpus": world, "steps": a.steps,
             "warmup": a.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": (value / world / PAGES_HEADLINE_TOKENS_PER_S) if a.workload == DEFAULT_WORKLOAD else None,
-            "dtype": "bf16/fp16 (fp32 accumulate, fp32 state and o)", "data": "synthetic", "config": workload_config(a.workload, inp),
+            "dtype": ("fp32 (bf16 q, k, v)" if decode else "bf16/fp16 (fp32 accumulate, fp32 state and o)"),
+            "data": "synthetic", "config": workload_config(a.workload, inp),
             "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": traffic,
                          "kernel": kernel, "algorithmic_bytes_per_launch": alg_bytes,
@@ -391,7 +401,7 @@ def bench_gpu(a, world, rank, local):
                         "p90": sorted(step_ms)[(9 * len(step_ms)) // 10]},
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "steps": e2e_steps},
-            "gpu_launches": a.steps * kda.chunk_fwd_launches(N, T, H),
+            "gpu_launches": a.steps * (1 if decode else kda.chunk_fwd_launches(N, T, H)),
             "clocks": clocks,
             "cpu_baseline": cpu,
         }

@@ -197,6 +197,42 @@ kda_status_t kda_chunk_fwd_debug(const void *q, const void *k, const void *v, co
                                  int32_t *status_dev, void *workspace, size_t workspace_bytes,
                                  kda_stream_t stream, uint32_t debug_flags);
 
+/*
+ * kda_decode_fwd — the KDA recurrence for a few tokens per sequence (decode /
+ * recurrent step), with the state carried in and out.
+ *
+ * Defined by the token recurrence above (report §1–§2), applied token after
+ * token:  S <- Diag(e^{g_t}) S;  S <- S + beta_t k_t (v_t^T - k_t^T S);
+ * o_t = scale * S^T q_t. It is the same operation kda_chunk_fwd computes, for
+ * batches of equally short sequences, where the chunked form has no chunk to
+ * work on: every sequence has exactly tokens_per_seq tokens.
+ *
+ * Inputs (device memory, row-major, contiguous; T = num_seqs * tokens_per_seq,
+ * the tokens of sequence n at rows n*tokens_per_seq .. n*tokens_per_seq + tokens_per_seq - 1):
+ *   q, k, v       bf16 [T, num_heads, 128]
+ *   g             fp32 [T, num_heads, 128] (natural-log decay, lower_bound <= g <= 0)
+ *   beta          fp32 [T, num_heads]
+ *   initial_state fp32 [num_seqs, num_heads, 128, 128] (key rows) or NULL for zeros
+ *   tokens_per_seq  0 .. KDA_DECODE_MAX_TOKENS (0: the state passes through)
+ * Outputs:
+ *   o             fp32 [T, num_heads, 128]
+ *   final_state   fp32 [num_seqs, num_heads, 128, 128] or NULL; may be the same
+ *                 pointer as initial_state (the usual in-place decode update)
+ *   status_dev    optional device int32, zeroed on the stream, then set to
+ *                 KDA_ERR_GATE_RANGE if some g lies outside [lower_bound, 0]
+ * Arithmetic is fp32 throughout. One launch; asynchronous on `stream`; nothing
+ * is allocated. Alignment: q, k, v, g, o and the states 16-byte aligned, beta
+ * and status_dev 4-byte aligned. Returns KDA_OK once queued, or a host-side
+ * error code with nothing launched. (The fused decode step of "Kimi K3 на
+ * графических процессорах AMD Instinct" §1.2 also folds in the short
+ * convolution and the output norm; those steps are outside this call.)
+ */
+#define KDA_DECODE_MAX_TOKENS 64
+kda_status_t kda_decode_fwd(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                            int32_t num_seqs, int32_t tokens_per_seq, int32_t num_heads, int32_t head_dim_k,
+                            int32_t head_dim_v, const float *initial_state, float scale, float lower_bound,
+                            float *o, float *final_state, int32_t *status_dev, kda_stream_t stream);
+
 /* Number of kernel launches one kda_chunk_fwd call makes for these sizes
  * (0 when num_seqs == 0). Host-only, no CUDA call. */
 int32_t kda_chunk_fwd_launches(int32_t num_seqs, int64_t total_tokens, int32_t num_heads);

@@ -29,7 +29,9 @@ KDA_DEBUG_WITHHOLD_READY = 1
 
 HEAD_DIM = 128
 EXPORTED = ("kda_chunk_fwd", "kda_chunk_fwd_workspace_size", "kda_chunk_fwd_static_scratch",
-            "kda_chunk_fwd_debug", "kda_chunk_fwd_launches", "kda_status_string", "kda_version")
+            "kda_chunk_fwd_debug", "kda_decode_fwd", "kda_chunk_fwd_launches", "kda_status_string",
+            "kda_version")
+DECODE_MAX_TOKENS = 64
 
 _lock = threading.Lock()
 _lib = None
@@ -63,6 +65,8 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.kda_chunk_fwd.restype = ctypes.c_int
         lib.kda_chunk_fwd_debug.argtypes = lib.kda_chunk_fwd.argtypes + [ctypes.c_uint32]
         lib.kda_chunk_fwd_debug.restype = ctypes.c_int
+        lib.kda_decode_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, f32, f32, vp, vp, vp, vp]
+        lib.kda_decode_fwd.restype = ctypes.c_int
         lib.kda_chunk_fwd_workspace_size.argtypes = [i32, i32]
         lib.kda_chunk_fwd_workspace_size.restype = ctypes.c_size_t
         lib.kda_chunk_fwd_launches.argtypes = [i32, i64, i32]
@@ -191,4 +195,67 @@ def chunk_fwd(q, k, v, g, beta, cu_seqlens, initial_state=None, scale: Optional[
         code = int(status.item())
         if code != KDA_OK:
             raise KdaError(code, "kda_chunk_fwd (device)")
+    return o, fs
+
+
+def kda_decode_fwd(q, k, v, g, beta, num_seqs: int, initial_state, scale: float, lower_bound: float,
+                   o, final_state, status=None, stream=None) -> int:
+    """Call the C entry point ``kda_decode_fwd`` with caller-allocated outputs.
+
+    q, k, v: bf16 [N*Tn, H, 128] (sequence n's Tn tokens at rows n*Tn..); g:
+    fp32 [N*Tn, H, 128]; beta: fp32 [N*Tn, H]; o: fp32 [N*Tn, H, 128];
+    initial_state / final_state: fp32 [N, H, 128, 128] or None (they may be
+    the same tensor). Raises ``KdaError`` on a host-side error.
+    """
+    T, H, D = q.shape
+    N = int(num_seqs)
+    if N < 0 or (N == 0 and T != 0) or (N > 0 and T % N != 0):
+        raise ValueError("q must hold the same number of tokens for every sequence")
+    Tn = T // N if N > 0 else 0
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    _check(q, "q", torch.bfloat16, (T, H, D), dev)
+    _check(k, "k", torch.bfloat16, (T, H, D), dev)
+    _check(v, "v", torch.bfloat16, (T, H, v.shape[2]), dev)
+    _check(g, "g", torch.float32, (T, H, D), dev)
+    _check(beta, "beta", torch.float32, (T, H), dev)
+    _check(o, "o", torch.float32, tuple(v.shape), dev)
+    if initial_state is not None:
+        _check(initial_state, "initial_state", torch.float32, (N, H, D, v.shape[2]), dev)
+    if final_state is not None:
+        _check(final_state, "final_state", torch.float32, (N, H, D, v.shape[2]), dev)
+    if status is not None:
+        _check(status, "status", torch.int32, (1,), dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    rc = load_library().kda_decode_fwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), N, Tn, H, D, v.shape[2], _ptr(initial_state),
+        float(scale), float(lower_bound), _ptr(o), _ptr(final_state), _ptr(status), ctypes.c_void_p(stream.cuda_stream))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_decode_fwd")
+    return rc
+
+
+def decode_fwd(q, k, v, g, beta, num_seqs: int, state=None, scale: Optional[float] = None,
+               lower_bound: float = -5.0, in_place: bool = False, check: bool = False, stream=None):
+    """Run ``kda_decode_fwd``; returns ``(o, final_state)``. With ``in_place``
+    the given ``state`` tensor is updated and returned as ``final_state``."""
+    T, H, D = q.shape
+    N = int(num_seqs)
+    if scale is None:
+        scale = D ** -0.5
+    o = torch.empty((T, H, v.shape[2]), dtype=torch.float32, device=q.device)
+    if in_place:
+        if state is None:
+            raise ValueError("in_place needs a state tensor")
+        fs = state
+    else:
+        fs = torch.empty((N, H, D, v.shape[2]), dtype=torch.float32, device=q.device)
+    status = torch.zeros(1, dtype=torch.int32, device=q.device) if check else None
+    kda_decode_fwd(q, k, v, g, beta, N, state, scale, lower_bound, o, fs, status, stream)
+    if check:
+        code = int(status.item())
+        if code != KDA_OK:
+            raise KdaError(code, "kda_decode_fwd (device)")
     return o, fs

@@ -47,6 +47,20 @@ def _stamp() -> str:
     return h.hexdigest()
 
 
+def kernel_stamp(source: str) -> str:
+    """Hash of one kernel's translation unit: its .cu file, the shared device
+    headers it can include, and the compile flags. A change elsewhere (another
+    kernel, the host API, documentation) leaves it unchanged."""
+    h = hashlib.sha256()
+    for f in [os.path.join(CSRC, source)] + sorted(glob.glob(os.path.join(CSRC, "*.cuh"))) + \
+            sorted(glob.glob(os.path.join(CSRC, "*.h"))):
+        h.update(os.path.relpath(f, ROOT).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    h.update(" ".join(ARCH + NVCC_FLAGS).encode())
+    return h.hexdigest()
+
+
 def build(force: bool = False, verbose: bool = False) -> str:
     """Compile and link; skipped when the sources are unchanged since the last build."""
     os.makedirs(BUILD_DIR, exist_ok=True)

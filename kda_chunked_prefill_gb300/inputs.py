@@ -42,6 +42,7 @@ class Workload:
     sigma_g: float = 1.0
     state_std: Optional[float] = None  # None: no initial state (zeros)
     lower_bound: float = -5.0
+    kind: str = "prefill"             # "decode": every sequence has the same few tokens
 
     def describe(self) -> dict:
         return dataclasses.asdict(self)
@@ -53,7 +54,7 @@ def _lognormal_lengths(rng, n: int) -> List[int]:
 
 
 def workloads() -> dict:
-    """The named workloads (tiny, headline, cached-prefix, batch sweep, wide)."""
+    """The named workloads (tiny, headline, cached-prefix, batch sweep, wide; decode steps)."""
     w = {
         "tiny_T256_H2": Workload("tiny_T256_H2", (256,), 1, 2, seed=0),
         "headline_4x2048_H16": Workload("headline_4x2048_H16", (2048,) * 4, 4, 16, seed=1),
@@ -66,6 +67,9 @@ def workloads() -> dict:
     }
     for b in (1, 2, 4, 8, 16, 32, 64):
         w[f"sweep_B{b}_H16"] = Workload(f"sweep_B{b}_H16", None, b, 16, seed=b)
+    # decode steps: one new token per sequence on a carried state
+    w["decode_B256_H16"] = Workload("decode_B256_H16", (1,) * 256, 256, 16, seed=9, state_std=0.02, kind="decode")
+    w["decode_B64x4_H16"] = Workload("decode_B64x4_H16", (4,) * 64, 64, 16, seed=10, state_std=0.02, kind="decode")
     return w
 
 

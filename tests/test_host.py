@@ -108,6 +108,37 @@ def test_debug_entry_validates_like_the_plain_call(lib):
                        beta=None, o=None, cu=None) == kda.KDA_OK
 
 
+def _call_decode(lib, **over):
+    fake = ctypes.c_void_p(0x10000)
+    args = dict(q=fake, k=fake, v=fake, g=fake, beta=fake, N=4, Tn=1, H=4, dk=128, dv=128, s0=None,
+                scale=0.088, lb=-5.0, o=fake, sT=fake, status=None, stream=None)
+    args.update(over)
+    return lib.kda_decode_fwd(args["q"], args["k"], args["v"], args["g"], args["beta"], args["N"], args["Tn"],
+                              args["H"], args["dk"], args["dv"], args["s0"], args["scale"], args["lb"], args["o"],
+                              args["sT"], args["status"], args["stream"])
+
+
+@pytest.mark.parametrize("over,code", [
+    ({"dk": 64}, kda.KDA_ERR_UNSUPPORTED),
+    ({"H": 0}, kda.KDA_ERR_INVALID_ARG),
+    ({"N": -1}, kda.KDA_ERR_INVALID_ARG),
+    ({"Tn": -1}, kda.KDA_ERR_INVALID_ARG),
+    ({"Tn": 65}, kda.KDA_ERR_INVALID_ARG),  # beyond KDA_DECODE_MAX_TOKENS
+    ({"lb": -11.0}, kda.KDA_ERR_INVALID_ARG),
+    ({"scale": float("nan")}, kda.KDA_ERR_INVALID_ARG),
+    ({"q": None}, kda.KDA_ERR_INVALID_ARG),
+    ({"o": None}, kda.KDA_ERR_INVALID_ARG),
+    ({"v": ctypes.c_void_p(0x10008)}, kda.KDA_ERR_INVALID_ARG),
+    ({"sT": ctypes.c_void_p(0x10004)}, kda.KDA_ERR_INVALID_ARG),
+])
+def test_decode_host_validation_rejects(lib, over, code):
+    assert _call_decode(lib, **over) == code
+
+
+def test_decode_with_no_sequences_is_a_no_op(lib):
+    assert _call_decode(lib, N=0, q=None, k=None, v=None, g=None, beta=None, o=None, sT=None) == kda.KDA_OK
+
+
 def test_workspace_size_is_zero_for_empty_problems(lib):
     assert kda.workspace_size(0, 4) == 0
     assert kda.workspace_size(3, 0) == 0
