@@ -81,6 +81,8 @@ __device__ __forceinline__ void cp_async16(void *dst, const void *src, int src_b
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
+// all but the most recent commit group of this thread have completed
+__device__ __forceinline__ void cp_async_wait_group1() { asm volatile("cp.async.wait_group 1;\n" ::: "memory"); }
 
 // ldmatrix: four 8x8 b16 matrices; lane l supplies the row address of
 // matrix l/8, row l%8.
@@ -205,31 +207,11 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         : "memory");
 }
 
-// Prefetch of a tensor box into L2 (no shared memory, no completion)
-__device__ __forceinline__ void tma_prefetch_l2_3d(const void *tmap, int x, int y, int z) {
-    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
-                     reinterpret_cast<uint64_t>(tmap)),
-                 "r"(x), "r"(y), "r"(z)
-                 : "memory");
-}
-
 // named barriers: `n` threads (a multiple of 32) of the CTA meet at barrier `id`
 __device__ __forceinline__ void named_bar_arrive(int id, int n) {
     asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 __device__ __forceinline__ void named_bar_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
-
-// Tiled 3-D tensor load (TMA) into this CTA's shared memory, completing on
-// `bar` (tx bytes = the full box). `tmap` is the address of a tensor map held
-// in a __grid_constant__ kernel parameter; x * element size must be a
-// multiple of 16 bytes; elements outside the tensor read as zero.
-__device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, int x, int y, int z, uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
-            smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
-        : "memory");
-}
 
 // 1-D bulk copy this CTA's shared memory -> global, tracked by the issuing
 // thread's bulk async-groups. Addresses 16-byte aligned, size a multiple of 16.

@@ -20,10 +20,6 @@
 // intra-chunk work (most of the arithmetic) is spread over every other SM.
 // All waits are bounded: a wait that runs out sets KDA_ERR_TIMEOUT and an abort
 // word in the workspace, and every CTA then returns.
-#include <cudaTypedefs.h>
-#include <string.h>
-
-#include <mutex>
 
 #include "kda.h"
 #include "kda_common.cuh"
@@ -222,7 +218,7 @@ __device__ __forceinline__ bool map_task(const Params &p, const int32_t *cu, int
 namespace prod {
 // q, k, v and their derived tiles are [64 tokens][128 channels] 16-bit tiles
 // and g is a [64][128] fp32 tile, all in the 128-byte-swizzled layout the
-// tensor copies write (16 KB and 32 KB; 1024-byte aligned).
+// input copies write (16 KB and 32 KB; 1024-byte aligned).
 constexpr int RSF = 136, RSA = 72;
 constexpr int SZ_T = BT * DK * 2;             // 16384
 constexpr int SZ_F = BT * RSF * 4;            // 34816 (kb keeps a padded row stride)
@@ -239,8 +235,7 @@ constexpr int OFF_T = OFF_LD + 4352;          // T = (I+L)^-1, fp16 [64][RSA] (l
 constexpr int OFF_TAB = OFF_T + SZ_A;         // per-channel tables, fp32 [20][128]
 constexpr int OFF_BETA = OFF_TAB + 10240;
 constexpr int OFF_MISC = OFF_BETA + 256;      // flags and the task broadcast (32 ints)
-constexpr int OFF_BAR = OFF_MISC + 128;       // input-load mbarriers: g, then q/k/v
-constexpr int OFF_CU = OFF_BAR + 16;          // copy of cu_seqlens when it has at most CU_CACHE entries
+constexpr int OFF_CU = OFF_MISC + 128;        // copy of cu_seqlens when it has at most CU_CACHE entries
 constexpr int CU_CACHE = 1024;
 constexpr int SMEM = OFF_CU + 4 * CU_CACHE;
 // Warp w runs on sub-partition w % 4. During the strips, warps 0-9 hold the
@@ -250,7 +245,7 @@ constexpr int SMEM = OFF_CU + 4 * CU_CACHE;
 constexpr int SYNC_TID = 13 * 32;             // lane 0 of warp 13: draws tasks
 constexpr int REL_TID = 12 * 32;              // lane 0 of warp 12: waits for free slots, stores and publishes images
 constexpr int TGM = 0, TGL = 4 * 128, TEM = 5 * 128, TEL = 9 * 128, TF = 13 * 128, TD = 19 * 128;
-static_assert(OFF_Q % 1024 == 0 && OFF_GKB % 1024 == 0, "tensor-copy destinations are 1024-byte aligned");
+static_assert(OFF_Q % 1024 == 0 && OFF_GKB % 1024 == 0, "swizzled tiles are 1024-byte aligned");
 // byte offset of the 16-byte chunk holding channels [c4, c4+4) of row r of the g tile
 __device__ __forceinline__ int g_chunk(int r, int c4) {
     return (c4 >> 5) * (BT * 128) + r * 128 + ((((c4 >> 2) & 7) ^ (r & 7)) << 4);
@@ -333,60 +328,45 @@ __device__ __forceinline__ Task fetch_task(const Params &p, const int32_t *cu, i
 }
 
 // One task's inputs into shared memory, called by all threads once the
-// buffers are free: q, k, v and g as ten tiled tensor copies issued by
-// SYNC_TID, g completing on `bar_g` and q, k, v on `bar_q` (one phase per
-// task each, so the prefix sum can start before q, k, v land), beta by
-// cp.async from warps 14 and 15.
-// Rows past the sequence end are zeroed once the copies have landed.
-__device__ __forceinline__ void issue_loads(const Params &p, unsigned char *smem, const Task &tk, uint64_t *bar_g,
-                                            uint64_t *bar_q) {
+// buffers are free: 16-byte cp.async copies into the 128-byte-swizzled tile
+// layouts, g (fp32) in a first commit group, q, k, v (bf16) and beta in a
+// second, so the prefix sum can start before q, k and v land. Rows past the
+// sequence end are zero-filled (g = 0 keeps row 63 of G at the last valid
+// prefix; k = v = beta = 0 rows are inert in every product).
+__device__ __forceinline__ void issue_loads(const Params &p, unsigned char *smem, const Task &tk) {
     const int tid = threadIdx.x;
-    const int h = tk.h;
-    const int64_t t0 = tk.t0;
-    const int nv = tk.nv;
-    if (tid == SYNC_TID) {
-        const int z = tk.t0;
-        mbar_arrive_expect_tx(bar_g, BT * DK * 4);
-        for (int qt = 0; qt < 4; ++qt) tma_load_3d(smem + OFF_GKB + qt * (BT * 128), &p.tm_g, 32 * qt, h, z, bar_g);
-        mbar_arrive_expect_tx(bar_q, 3 * SZ_T);
-        for (int half = 0; half < 2; ++half) {
-            tma_load_3d(smem + OFF_Q + half * (SZ_T / 2), &p.tm_q, 64 * half, h, z, bar_q);
-            tma_load_3d(smem + OFF_K + half * (SZ_T / 2), &p.tm_k, 64 * half, h, z, bar_q);
-            tma_load_3d(smem + OFF_V + half * (SZ_T / 2), &p.tm_v, 64 * half, h, z, bar_q);
-        }
-        KDA_TRACE_ANY(p, 30, 0);
+    const size_t rs = static_cast<size_t>(p.H) * DK;  // token stride, elements
+    const size_t hb = static_cast<size_t>(tk.h) * DK;
+    KDA_TRACE_EV(p, 30, 0);
+#pragma unroll
+    for (int it = 0; it < BT * 32 / NCOMP; ++it) {  // g: 64 rows x 32 chunks of 4 channels
+        const int idx = tid + it * NCOMP, r = idx >> 5, c4 = (idx & 31) << 2;
+        const bool ok = r < tk.nv;
+        cp_async16(smem + OFF_GKB + g_chunk(r, c4), p.g + static_cast<size_t>(tk.t0 + (ok ? r : 0)) * rs + hb + c4,
+                   ok ? 16 : 0);
     }
-    if (tid >= NCOMP - BT) {  // warps 14 and 15: off the critical path after the strips
+    cp_async_commit();
+#pragma unroll
+    for (int it = 0; it < BT * 16 / NCOMP; ++it) {  // q, k, v: 64 rows x 16 chunks of 8 channels
+        const int idx = tid + it * NCOMP, r = idx >> 4, c8 = (idx & 15) << 3;
+        const bool ok = r < tk.nv;
+        const size_t off = static_cast<size_t>(tk.t0 + (ok ? r : 0)) * rs + hb + c8;
+        const int d = tile_chunk(64, r, c8);
+        cp_async16(smem + OFF_Q + d, p.q + off, ok ? 16 : 0);
+        cp_async16(smem + OFF_K + d, p.k + off, ok ? 16 : 0);
+        cp_async16(smem + OFF_V + d, p.v + off, ok ? 16 : 0);
+    }
+    if (tid >= NCOMP - BT) {  // warps 14 and 15
         const int r = tid - (NCOMP - BT);
-        const bool ok = r < nv;
-        cp_async4(smem + OFF_BETA + 4 * r, p.beta + static_cast<size_t>(t0 + (ok ? r : 0)) * p.H + h, ok ? 4 : 0);
-        cp_async_commit();
+        const bool ok = r < tk.nv;
+        cp_async4(smem + OFF_BETA + 4 * r, p.beta + static_cast<size_t>(tk.t0 + (ok ? r : 0)) * p.H + tk.h, ok ? 4 : 0);
     }
-}
-
-// rows >= nv of the input tiles (the tensor copies read the next sequence
-// there): zero, so that padded tokens contribute nothing and g = 0 keeps
-// row 63 of G at the last valid prefix
-__device__ __forceinline__ void zero_tail(unsigned char *smem, const Task &tk) {
-    const int nv = tk.nv;
-    for (int idx = nv * 8 + threadIdx.x; idx < BT * 8; idx += NCOMP) {  // whole 128-byte rows
-        const int r = idx >> 3, c = (idx & 7) << 4;
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            const int off = half * (SZ_T / 2) + r * 128 + c;
-            *reinterpret_cast<uint4 *>(smem + OFF_Q + off) = make_uint4(0, 0, 0, 0);
-            *reinterpret_cast<uint4 *>(smem + OFF_K + off) = make_uint4(0, 0, 0, 0);
-            *reinterpret_cast<uint4 *>(smem + OFF_V + off) = make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int qt = 0; qt < 4; ++qt)
-            *reinterpret_cast<uint4 *>(smem + OFF_GKB + qt * (BT * 128) + r * 128 + c) = make_uint4(0, 0, 0, 0);
-    }
+    cp_async_commit();
 }
 
 // One (chain, chunk) task: steps 1-4 into the slot image, then the bulk store
 // of the image into the task's slot. Its inputs were loaded by issue_loads.
-// `nxt` is the next task (drawn one task earlier); its tensor copies start
+// `nxt` is the next task (drawn one task earlier); its input copies start
 // right after the strips.
 // During the strips, REL_TID completes and publishes the previous task's slot
 // (`pending` = its ready-flag index or -1, `pending_val` the value) while
@@ -398,8 +378,7 @@ __device__ __forceinline__ void zero_tail(unsigned char *smem, const Task &tk) {
 // Returns false when the slot wait gave up (timeout or abort).
 __device__ __forceinline__ bool run_task(const Params &p, const Ring &Rg, unsigned char *smem, const Task &cur,
                                          const int32_t *cu_s, int jmax, const Task &nxt, Task &nxt2, Cursor &cs, int &pending,
-                                         int pending_val, uint64_t *bar_g, uint64_t *bar_q, uint32_t ph,
-                                         int &landed_q, int &issued, bool &gate_bad, bool &range_bad) {
+                                         int pending_val, bool &gate_bad, bool &range_bad) {
     unsigned char *img = smem + OFF_IMG;
     unsigned char *sQ = smem + OFF_Q, *sK = smem + OFF_K, *sV = smem + OFF_V;
     unsigned char *sGb = smem + OFF_GKB;  // G, swizzled (g_chunk / g_elem)
@@ -458,9 +437,8 @@ __device__ __forceinline__ bool run_task(const Params &p, const Ring &Rg, unsign
             for (int j = 0; j < i; ++j) sTab[TF + f_pair(i, j) * 128 + chn] = ex2(gm[i] - gm[j]);
     }
     if (tid == REL_TID) bulk_wait_read();  // the previous image has been read out and may be rewritten
-    const bool q_landed = wait_mbar(Rg, bar_q, ph, p.status);
-    if (__syncthreads_or(!q_landed)) return false;  // one decision for the whole CTA
-    ++landed_q;
+    cp_async_wait_all();  // q, k, v and beta
+    sync_compute();
     KDA_TRACE_EV(p, 21, 0);
 
     // ---- steps 2a/4a: elementwise operands; q_hat, kg, beta*v and
@@ -678,10 +656,7 @@ __device__ __forceinline__ bool run_task(const Params &p, const Ring &Rg, unsign
     nxt2 = get_task(misc + 2);
     const bool slot_ok = misc[20] != 0;
     // q, k, v, q*a lo, kb and beta are free: stream in the next task
-    if (nxt.valid) {
-        issue_loads(p, smem, nxt, bar_g, bar_q);
-        ++issued;
-    }
+    if (nxt.valid) issue_loads(p, smem, nxt);
     if (!slot_ok) return false;
     KDA_TRACE_EV(p, 23, 0);
 
@@ -790,13 +765,6 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int pi
         const int j = tile < 3 ? tile + 1 : (tile < 5 ? tile - 1 : 3);
         *reinterpret_cast<uint32_t *>(smem + OFF_IMG + SL_AQK + tile_elem(64, 16 * i + rr, 16 * j + cc)) = 0u;
     }
-    uint64_t *bar_g = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
-    uint64_t *bar_q = bar_g + 1;
-    if (tid == 0) {
-        mbar_init(bar_g, 1);
-        mbar_init(bar_q, 1);
-        mbar_fence_init();
-    }
     sync_compute();
     const int jmax = misc[1];
     Cursor cs = make_cursor(pid, static_cast<int>(gridDim.x) - p.C, p.C);  // used by SYNC_TID
@@ -810,27 +778,16 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int pi
     Task cur = get_task(misc + 2);
     Task nxt = get_task(misc + 10);
     sync_compute();
-    int issued = 0, landed_g = 0, landed_q = 0;  // load phases, the same in every thread
-    if (cur.valid) {
-        issue_loads(p, smem, cur, bar_g, bar_q);
-        ++issued;
-    }
+    if (cur.valid) issue_loads(p, smem, cur);
     bool gate_bad = false, range_bad = false;
     int pending = -1, pending_val = 0;  // REL_TID: the last slot stored but not yet published
     while (cur.valid) {
         KDA_TRACE_EV(p, 1, cur.j * p.C + cur.k);
-        const uint32_t ph = static_cast<uint32_t>(landed_g) & 1u;
-        cp_async_wait_all();
-        bool ok = wait_mbar(R, bar_g, ph, p.status);
-        if (cur.nv < BT) ok = ok && wait_mbar(R, bar_q, ph, p.status);  // a tail's rows are zeroed after both
-        if (__syncthreads_or(!ok)) break;  // one decision for the whole CTA
-        ++landed_g;
-        if (cur.nv < BT) zero_tail(smem, cur);
+        cp_async_wait_group1();  // g (q, k, v and beta may still be in flight)
         sync_compute();
         KDA_TRACE_EV(p, 20, 0);
         Task nxt2{0, 0, 0, 0, 0, 0, 0, 0};
-        if (!run_task(p, R, smem, cur, cu_s, jmax, nxt, nxt2, cs, pending, pending_val, bar_g, bar_q, ph, landed_q, issued,
-                      gate_bad, range_bad))
+        if (!run_task(p, R, smem, cur, cu_s, jmax, nxt, nxt2, cs, pending, pending_val, gate_bad, range_bad))
             break;
         if (tid == REL_TID) {
             pending = cur.k * RING + cur.j % RING;
@@ -840,9 +797,6 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int pi
         cur = nxt;
         nxt = nxt2;
     }
-    // after an abort: let this CTA's own tensor copies land before it leaves
-    for (; landed_g < issued; ++landed_g) drain_mbar(bar_g, static_cast<uint32_t>(landed_g) & 1u);
-    for (; landed_q < issued; ++landed_q) drain_mbar(bar_q, static_cast<uint32_t>(landed_q) & 1u);
     if (tid == REL_TID) {
         bulk_wait_all();
         if (pending >= 0) {
@@ -1184,36 +1138,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_persistent_kernel(const __gri
 }
 
 // ------------------------------------------------------------------ host side
-// cuTensorMapEncodeTiled, looked up once through the runtime (no link-time
-// dependence on the driver library)
-static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    });
-    return fn;
-}
-
-// [T][H][128] tensor, box = `box_c` channels x 1 head x 64 tokens, 128-byte swizzle
-static bool encode_input_map(CUtensorMap *m, const void *base, bool fp32, int64_t T, int32_t H, uint32_t box_c) {
-    const PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
-    if (!fn) return false;
-    const cuuint64_t esz = fp32 ? 4 : 2;
-    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(DK), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(T)};
-    const cuuint64_t strides[2] = {DK * esz, static_cast<cuuint64_t>(H) * DK * esz};
-    const cuuint32_t box[3] = {box_c, 1, static_cast<cuuint32_t>(BT)};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    return fn(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base),
-              dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 static int num_sms() {
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -1251,12 +1175,6 @@ cudaError_t launch(Params p, size_t ws_bytes, cudaStream_t stream) {
     const int grid = sms;  // one CTA per SM; all co-resident (cooperative launch)
     p.C = consumers_for(static_cast<int64_t>(p.N) * p.H, grid);
     p.spin = p.debug ? SPIN_LIMIT_DEBUG : SPIN_LIMIT;
-    memset(&p.tm_q, 0, sizeof(CUtensorMap) * 4);
-    if (p.T > 0) {  // with no tokens there are no producer tasks and no loads
-        if (!encode_input_map(&p.tm_q, p.q, false, p.T, p.H, 64) || !encode_input_map(&p.tm_k, p.k, false, p.T, p.H, 64) ||
-            !encode_input_map(&p.tm_v, p.v, false, p.T, p.H, 64) || !encode_input_map(&p.tm_g, p.g, true, p.T, p.H, 32))
-            return cudaErrorInvalidValue;
-    }
     if (ws_bytes < ring_offset(p.C) + static_cast<size_t>(p.C) * RING * SLOT_BYTES) return cudaErrorInvalidValue;
     e = cudaMemsetAsync(p.ws, 0, ring_offset(p.C), stream);
     if (e != cudaSuccess) return e;

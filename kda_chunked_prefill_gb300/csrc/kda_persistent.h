@@ -1,6 +1,5 @@
 // Internal interface of the persistent producer/consumer kernel (not part of the C ABI).
 #pragma once
-#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
@@ -13,9 +12,6 @@ constexpr int RING = 4;              // ring slots per consumer
 constexpr int SLOT_BYTES = 74752;    // one (chain, chunk) hand-off, 1024-byte multiple
 
 struct Params {
-    // TMA descriptors of q, k, v (bf16) and g (fp32) as [T][H][128] tensors,
-    // boxes of 64 channels (32 for g) x 1 head x 64 tokens, 128-byte swizzle
-    CUtensorMap tm_q, tm_k, tm_v, tm_g;
     const __nv_bfloat16 *q, *k, *v;
     const float *g, *beta;
     const int32_t *cu;
