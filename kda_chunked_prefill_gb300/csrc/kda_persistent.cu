@@ -85,7 +85,7 @@ __device__ __forceinline__ void trace_any(const Params &p, int tag, int value) {
     unsigned long long t;
     asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
     const int w = threadIdx.x >> 5;
-    unsigned char *base = p.ws + ring_offset(p.C) + static_cast<size_t>(p.C) * RING * SLOT_BYTES;
+    unsigned char *base = p.ws + ring_offset(p.Cws) + static_cast<size_t>(p.Cws) * RING * SLOT_BYTES;
     unsigned long long *rec = reinterpret_cast<unsigned long long *>(base) + blockIdx.x * TRACE_CTA_WORDS;
     const int n = cnt[w];
     if (n < TRACE_EVENTS) {
@@ -1145,17 +1145,52 @@ static int num_sms() {
     return sms;
 }
 
-int consumers_for(int64_t chains, int grid) {
+// Most consumer CTAs a launch uses (half the SMs, at most one per chain): the
+// workspace is sized for this many rings.
+int max_consumers(int64_t chains, int grid) {
     int64_t c = grid / 2;
     if (c < 1) c = 1;
     if (chains < c) c = chains;
     return static_cast<int>(c < 1 ? 1 : c);
 }
 
+// Consumer CTAs for one launch, from a cost model of the two roles: a consumer
+// that is kept busy completes about one chunk per 3.5 us (2.45 us of its own
+// work; the rest is the ring's hand-off latency with four slots), a producer
+// about one chunk per 7.0 us, and the launch takes the longer of
+//   (chains per consumer) x (chunks per chain) x 3.5 us   and
+//   (all chunks) x 7.0 us / (producer CTAs).
+// Candidates give every consumer the same number of chains (C = ceil(chains / m)).
+// `tokens` sizes the chunk count (each sequence adds at most one partial chunk).
+int consumers_for(int64_t chains, int64_t tokens, int64_t seqs, int grid) {
+    const int cmax = max_consumers(chains, grid);
+    if (chains < 1 || grid < 2) return cmax;
+    constexpr double T_CONS = 3.5, T_PROD = 7.0;  // us per chunk, measured on GB300
+    const double chunks = static_cast<double>(chains / (seqs > 0 ? seqs : 1)) *
+                          (static_cast<double>(tokens) / BT + 0.5 * static_cast<double>(seqs));
+    const double per_chain = chunks / static_cast<double>(chains);
+    int best = cmax;
+    double best_cost = 1e300;
+    for (int64_t m = 1;; ++m) {
+        const int64_t c = (chains + m - 1) / m;
+        if (c <= cmax && c < grid) {
+            const double cons = static_cast<double>((chains + c - 1) / c) * per_chain * T_CONS;
+            const double prod = chunks * T_PROD / static_cast<double>(grid - c);
+            const double cost = cons > prod ? cons : prod;
+            if (cost < best_cost) {
+                best_cost = cost;
+                best = static_cast<int>(c);
+            }
+        }
+        if (c <= 1) break;
+    }
+    return best;
+}
+
 size_t workspace_bytes(int64_t chains) {
     const int sms = num_sms();
     if (sms < 2 || chains < 1) return 0;
-    const int C = consumers_for(chains, sms);
+    const int C = max_consumers(chains, sms);
     size_t bytes = ring_offset(C) + static_cast<size_t>(C) * RING * SLOT_BYTES;
 #ifdef KDA_TRACE
     bytes += static_cast<size_t>(sms) * TRACE_CTA_WORDS * 8;
@@ -1173,13 +1208,15 @@ cudaError_t launch(Params p, size_t ws_bytes, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     const int grid = sms;  // one CTA per SM; all co-resident (cooperative launch)
-    p.C = consumers_for(static_cast<int64_t>(p.N) * p.H, grid);
+    const int64_t chains = static_cast<int64_t>(p.N) * p.H;
+    p.C = consumers_for(chains, p.T, p.N, grid);
+    p.Cws = max_consumers(chains, grid);
     p.spin = p.debug ? SPIN_LIMIT_DEBUG : SPIN_LIMIT;
-    if (ws_bytes < ring_offset(p.C) + static_cast<size_t>(p.C) * RING * SLOT_BYTES) return cudaErrorInvalidValue;
+    if (ws_bytes < ring_offset(p.Cws) + static_cast<size_t>(p.Cws) * RING * SLOT_BYTES) return cudaErrorInvalidValue;
     e = cudaMemsetAsync(p.ws, 0, ring_offset(p.C), stream);
     if (e != cudaSuccess) return e;
 #ifdef KDA_TRACE
-    e = cudaMemsetAsync(p.ws + ring_offset(p.C) + static_cast<size_t>(p.C) * RING * SLOT_BYTES, 0,
+    e = cudaMemsetAsync(p.ws + ring_offset(p.Cws) + static_cast<size_t>(p.Cws) * RING * SLOT_BYTES, 0,
                         static_cast<size_t>(grid) * TRACE_CTA_WORDS * 8, stream);
     if (e != cudaSuccess) return e;
 #endif

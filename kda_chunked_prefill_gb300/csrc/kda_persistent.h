@@ -24,6 +24,7 @@ struct Params {
     int32_t *status;
     unsigned char *ws;
     int32_t C;           // consumer CTAs (set by launch)
+    int32_t Cws;         // consumers the workspace rings were sized for (>= C)
     uint32_t debug;      // KDA_DEBUG_* flags (0 in normal calls)
     long long spin;      // polls before a wait gives up
 };
@@ -33,7 +34,8 @@ __host__ __device__ constexpr size_t ring_offset(int C) {
     return ((64 + 8 * static_cast<size_t>(C) * RING) + 1023) / 1024 * 1024;
 }
 
-int consumers_for(int64_t chains, int grid);
+int max_consumers(int64_t chains, int grid);
+int consumers_for(int64_t chains, int64_t tokens, int64_t seqs, int grid);
 size_t workspace_bytes(int64_t chains);
 cudaError_t launch(Params p, size_t ws_bytes, cudaStream_t stream);
 
