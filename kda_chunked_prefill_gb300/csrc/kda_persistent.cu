@@ -179,20 +179,154 @@ __device__ __forceinline__ int chain_info(const Params &p, const int32_t *cu, in
     return static_cast<int>((len + BT - 1) / BT);
 }
 
-// consumer k owns chains k, k + C, k + 2C, ...; its chunks form one sequence
-__device__ __forceinline__ int consumer_total(const Params &p, const int32_t *cu, int k) {
+// ------------------------------------------------------------ chain schedule
+// Which chains each consumer runs, in order. When every sequence has the same
+// number of chunks, consumer k takes chains k, k + C, k + 2C, ... (no table).
+// Otherwise, for at most SCHED_MAX_CHAINS chains, every CTA builds the same
+// table at start-up (deterministically, in shared memory): sequences in
+// decreasing order of their chunk count hand their H chains to the H consumers
+// with the least work so far (ties to the lower index), the longest-first
+// greedy rule, so that unequal lengths do not leave one consumer with most of
+// the work. order[cstart[k] .. cstart[k + 1]) lists consumer k's chains.
+// The same region keeps a copy of cu_seqlens (when it has at most CU_CACHE
+// entries) for both roles: the ring's acquire loads invalidate L1, so global
+// reads of it would go to L2 on every task.
+constexpr int SCHED_MAX_CHAINS = 1024, SCHED_MAX_C = 160, CU_CACHE = 1024;
+constexpr int SCHED_CU = 16 + 4 * (SCHED_MAX_C + 1) + 4 * SCHED_MAX_CHAINS;  // byte offset of the cu copy
+constexpr int SCHED_BYTES = SCHED_CU + 4 * CU_CACHE;
+// The schedule sits at OFF_SCHED of every CTA's shared memory, past both roles'
+// tiles: int flags[4] (table present, cu copy present), cstart, order, cu copy.
+constexpr int OFF_SCHED = 215168;  // = the consumer's tiles, the larger role (checked below)
+__device__ __forceinline__ const int *sched_flags(const unsigned char *smem) {
+    return reinterpret_cast<const int *>(smem + OFF_SCHED);
+}
+// cu_seqlens: the shared-memory copy, or p.cu
+__device__ __forceinline__ const int32_t *sched_cu(const Params &p, const unsigned char *smem) {
+    return sched_flags(smem)[1] ? reinterpret_cast<const int32_t *>(smem + OFF_SCHED + SCHED_CU) : p.cu;
+}
+// number of chains of consumer k, and its r-th chain
+__device__ __forceinline__ int sched_count(const Params &p, const unsigned char *smem, int k) {
+    const int *f = sched_flags(smem);
+    return f[0] ? f[4 + k + 1] - f[4 + k] : (p.N * p.H - k + p.C - 1) / p.C;
+}
+__device__ __forceinline__ int sched_chain(const Params &p, const unsigned char *smem, int k, int r) {
+    const int *f = sched_flags(smem);
+    return f[0] ? f[4 + SCHED_MAX_C + 1 + f[4 + k] + r] : k + r * p.C;
+}
+
+// Builds the schedule into `sched` on all threads of the CTA; `scratch` (at
+// least 8 KB + 8 * SCHED_MAX_CHAINS bytes) is free shared memory for the duration.
+__device__ void build_sched(const Params &p, unsigned char *sched, unsigned char *scratch) {
+    const int tid = threadIdx.x, nthr = blockDim.x;
+    const int N = p.N, H = p.H, C = p.C, chains = N * H;
+    int *flag = reinterpret_cast<int *>(sched);
+    int *cstart = flag + 4, *order = cstart + SCHED_MAX_C + 1;
+    const bool cache_cu = N + 1 <= CU_CACHE;
+    int32_t *cuc = reinterpret_cast<int32_t *>(sched + SCHED_CU);
+    int *nchk = reinterpret_cast<int *>(scratch);          // chunks per sequence
+    int *sorted = nchk + SCHED_MAX_CHAINS;                   // sequences by decreasing chunks
+    int *load = sorted + SCHED_MAX_CHAINS;                   // chunks given to each consumer
+    int *cnt = load + SCHED_MAX_C;                           // chains given to each consumer
+    int *asg = cnt + SCHED_MAX_C;                            // per chain: consumer << 16 | position
+    const bool fits = chains <= SCHED_MAX_CHAINS && C <= SCHED_MAX_C && N > 0;
+    // warp 0: copy cu_seqlens and find whether the sequences differ in chunk count
+    if (tid < 32) {
+        bool uneq = false;
+        int first = 0;
+        for (int n0 = 0; n0 <= N; n0 += 32) {
+            const int n = n0 + tid;
+            int32_t b = 0, e = 0;
+            if (n <= N) {
+                b = p.cu[n];
+                if (cache_cu) cuc[n] = b;
+            }
+            if (n < N) e = p.cu[n + 1];
+            const int nc = (n < N && e > b && b >= 0) ? static_cast<int>((static_cast<int64_t>(e) - b + BT - 1) / BT) : 0;
+            if (n0 == 0) first = __shfl_sync(0xffffffffu, nc, 0);
+            if (fits && n < N) nchk[n] = nc;
+            uneq |= __any_sync(0xffffffffu, n < N && nc != first);
+        }
+        if (tid == 0) {
+            flag[0] = (fits && uneq) ? 1 : 0;
+            flag[1] = cache_cu ? 1 : 0;
+        }
+    }
+    __syncthreads();
+    if (!flag[0]) return;
+    for (int n = tid; n < N; n += nthr) {
+        int r = 0;
+        for (int m = 0; m < N; ++m) r += (nchk[m] > nchk[n]) || (nchk[m] == nchk[n] && m < n);
+        sorted[r] = n;
+    }
+    for (int k = tid; k < C; k += nthr) {
+        load[k] = 0;
+        cnt[k] = 0;
+    }
+    __syncthreads();
+    for (int i = 0; i < N; ++i) {
+        const int n = sorted[i], w = nchk[n];
+        for (int h0 = 0; h0 < H; h0 += C) {  // the sequence's chains, at most C at a time
+            const int take = H - h0 < C ? H - h0 : C;
+            int rk = C;
+            if (tid < C) {
+                const int lk = load[tid];
+                rk = 0;
+                for (int m = 0; m < C; ++m) rk += (load[m] < lk) || (load[m] == lk && m < tid);
+            }
+            __syncthreads();
+            if (tid < C && rk < take) {
+                asg[n * H + h0 + rk] = (tid << 16) | cnt[tid];
+                ++cnt[tid];
+                load[tid] += w;
+            }
+            __syncthreads();
+        }
+    }
+    if (tid == 0) {
+        int acc = 0;
+        for (int k = 0; k < C; ++k) {
+            cstart[k] = acc;
+            acc += cnt[k];
+        }
+        cstart[C] = acc;
+    }
+    __syncthreads();
+    for (int ch = tid; ch < chains; ch += nthr) order[cstart[asg[ch] >> 16] + (asg[ch] & 0xffff)] = ch;
+    __syncthreads();
+}
+
+// total chunks of consumer k (its chains' chunks form one sequence)
+__device__ __forceinline__ int consumer_total(const Params &p, const unsigned char *sc, const int32_t *cu, int k) {
     int tot = 0;
-    for (int ch = k; ch < p.N * p.H; ch += p.C) {
-        int64_t b, l;
-        const int nc = chain_info(p, cu, ch, b, l);
+    int64_t b, l;
+    if (!sched_flags(sc)[0]) {
+        for (int ch = k; ch < p.N * p.H; ch += p.C) {
+            const int nc = chain_info(p, cu, ch, b, l);
+            tot += nc > 0 ? nc : 0;
+        }
+        return tot;
+    }
+    const int nchains = sched_count(p, sc, k);
+    for (int r = 0; r < nchains; ++r) {
+        const int nc = chain_info(p, cu, sched_chain(p, sc, k, r), b, l);
         tot += nc > 0 ? nc : 0;
     }
     return tot;
 }
 
-__device__ __forceinline__ bool map_task(const Params &p, const int32_t *cu, int k, int j, int &ch_out, int &c_out,
-                                         int64_t &bos, int64_t &len) {
-    for (int ch = k; ch < p.N * p.H; ch += p.C) {
+// chunk j of consumer k: its chain, the chunk's index in the chain and the chain's bounds
+__device__ __forceinline__ bool map_task(const Params &p, const unsigned char *sc, const int32_t *cu, int k, int j, int &ch_out,
+                                         int &c_out, int64_t &bos, int64_t &len) {
+    const bool table = sched_flags(sc)[0] != 0;
+    const int *row = sched_flags(sc) + 4 + SCHED_MAX_C + 1 + (table ? sched_flags(sc)[4 + k] : 0);
+    const int nchains = table ? sched_count(p, sc, k) : 0;
+    for (int r = 0, ch = k;; ++r, ch += p.C) {
+        if (table) {
+            if (r >= nchains) return false;
+            ch = row[r];
+        } else if (ch >= p.N * p.H) {
+            return false;
+        }
         int64_t b, l;
         int nc = chain_info(p, cu, ch, b, l);
         if (nc < 0) nc = 0;
@@ -205,7 +339,6 @@ __device__ __forceinline__ bool map_task(const Params &p, const int32_t *cu, int
         }
         j -= nc;
     }
-    return false;
 }
 
 // ================================================================== producer
@@ -235,9 +368,7 @@ constexpr int OFF_T = OFF_LD + 4352;          // T = (I+L)^-1, fp16 [64][RSA] (l
 constexpr int OFF_TAB = OFF_T + SZ_A;         // per-channel tables, fp32 [20][128]
 constexpr int OFF_BETA = OFF_TAB + 10240;
 constexpr int OFF_MISC = OFF_BETA + 256;      // flags and the task broadcast (32 ints)
-constexpr int OFF_CU = OFF_MISC + 128;        // copy of cu_seqlens when it has at most CU_CACHE entries
-constexpr int CU_CACHE = 1024;
-constexpr int SMEM = OFF_CU + 4 * CU_CACHE;
+constexpr int SMEM = OFF_MISC + 128;
 // Warp w runs on sub-partition w % 4. During the strips, warps 0-9 hold the
 // ten tiles (three on partitions 0 and 1, two on 2 and 3); the diagonal
 // inverses run on warps 10, 11, 14, 15 (partitions 2 and 3) and the ring work,
@@ -303,7 +434,7 @@ struct Cursor {
 __device__ __forceinline__ Cursor make_cursor(int pid, int P, int C) { return Cursor{pid % C, pid / C, P % C, P / C}; }
 
 // next valid task of the cursor (numbers whose consumer has fewer chunks are skipped)
-__device__ __forceinline__ Task fetch_task(const Params &p, const int32_t *cu, int jmax, Cursor &cs) {
+__device__ __forceinline__ Task fetch_task(const Params &p, const unsigned char *sc, const int32_t *cu, int jmax, Cursor &cs) {
     Task t{0, 0, 0, 0, 0, 0, 0, 0};
     while (cs.j < jmax) {
         t.k = cs.k;
@@ -315,7 +446,7 @@ __device__ __forceinline__ Task fetch_task(const Params &p, const int32_t *cu, i
             ++cs.j;
         }
         int64_t bos, len;
-        if (map_task(p, cu, t.k, t.j, t.ch, t.c, bos, len)) {
+        if (map_task(p, sc, cu, t.k, t.j, t.ch, t.c, bos, len)) {
             const int64_t t0 = bos + static_cast<int64_t>(t.c) * BT;
             t.t0 = static_cast<int>(t0);
             t.nv = static_cast<int>((bos + len - t0) < BT ? (bos + len - t0) : BT);
@@ -552,7 +683,7 @@ __device__ __forceinline__ bool run_task(const Params &p, const Ring &Rg, unsign
         KDA_TRACE_ANY(p, 33, 0);
     }
     if (tid == SYNC_TID) {
-        const Task t = fetch_task(p, cu_s, jmax, cs);
+        const Task t = fetch_task(p, smem, cu_s, jmax, cs);
         put_task(misc + 2, t);
         KDA_TRACE_ANY(p, 35, 0);
     }
@@ -742,20 +873,13 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int pi
     const int tid = threadIdx.x;
     Ring R = ring_of(p);
     int *misc = reinterpret_cast<int *>(smem + OFF_MISC);
-    // sequence bounds in shared memory (the ring's acquire loads invalidate L1,
-    // so global reads of them would go to L2 on every task)
-    const int32_t *cu_s = p.cu;
-    if (p.N + 1 <= CU_CACHE) {
-        int32_t *c = reinterpret_cast<int32_t *>(smem + OFF_CU);
-        for (int i = tid; i <= p.N; i += NCOMP) c[i] = p.cu[i];
-        cu_s = c;
-    }
+    const int32_t *cu_s = sched_cu(p, smem);  // sequence bounds (in shared memory when small enough)
     // longest consumer sequence: tasks beyond it do not exist
     if (tid == 0) misc[1] = 0;
     sync_compute();
     {
         int mx = 0;
-        for (int k = tid; k < p.C; k += NCOMP) mx = max(mx, consumer_total(p, cu_s, k));
+        for (int k = tid; k < p.C; k += NCOMP) mx = max(mx, consumer_total(p, smem, cu_s, k));
         atomicMax(&misc[1], mx);
     }
     // the upper 16x16 tiles of scale*Aqk are never written: zero them once
@@ -769,9 +893,9 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int pi
     const int jmax = misc[1];
     Cursor cs = make_cursor(pid, static_cast<int>(gridDim.x) - p.C, p.C);  // used by SYNC_TID
     if (tid == SYNC_TID) {
-        const Task t = fetch_task(p, cu_s, jmax, cs);
+        const Task t = fetch_task(p, smem, cu_s, jmax, cs);
         put_task(misc + 2, t);
-        const Task u = fetch_task(p, cu_s, jmax, cs);
+        const Task u = fetch_task(p, smem, cu_s, jmax, cs);
         put_task(misc + 10, u);
     }
     sync_compute();
@@ -876,7 +1000,8 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
     const uint32_t tmem = *tslot;
     const uint32_t tS = tmem + (static_cast<uint32_t>(32 * quad) << 16) + 32 * slice;  // this thread's S columns
     const uint32_t tD = tS + 128;                                                       // this thread's D columns
-    const int total = consumer_total(p, p.cu, k);
+    const int32_t *cu_s = sched_cu(p, smem);
+    const int total = consumer_total(p, smem, cu_s, k);
 
     auto issue = [&](int jj) {  // slot jj -> buffer jj % 2 (thread 0)
         const unsigned char *src = R.slots + static_cast<size_t>(k * RING + jj % RING) * SLOT_BYTES;
@@ -900,9 +1025,11 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
 
     int j = 0;
     bool range_bad = false, alive = true;
-    for (int ch = k; ch < p.N * p.H && alive; ch += p.C) {
+    const int nchains = sched_count(p, smem, k);
+    for (int r = 0; r < nchains && alive; ++r) {
+        const int ch = sched_chain(p, smem, k, r);
         int64_t bos, len;
-        const int nc = chain_info(p, p.cu, ch, bos, len);
+        const int nc = chain_info(p, cu_s, ch, bos, len);
         if (nc < 0) {
             if (tid == 0) set_status(p.status, KDA_ERR_BAD_SEQLENS);
             continue;
@@ -1115,7 +1242,9 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
 }
 }  // namespace cons
 
-constexpr int SMEM_TILES = (prod::SMEM > cons::SMEM ? prod::SMEM : cons::SMEM) + 1024;  // + alignment slack
+static_assert(prod::SMEM <= OFF_SCHED && cons::SMEM <= OFF_SCHED, "the chain schedule lies past both roles' tiles");
+constexpr int SMEM_TILES = OFF_SCHED + SCHED_BYTES + 1024;  // + alignment slack
+static_assert(8192 + 8 * SCHED_MAX_CHAINS + 8 * SCHED_MAX_C <= OFF_SCHED, "schedule scratch fits below the schedule");
 #ifdef KDA_TRACE
 static_assert(SMEM_TILES <= TRACE_COUNTS_OFFSET, "trace counters past the tiles");
 constexpr int SMEM_MAX = TRACE_COUNTS_OFFSET + 64;
@@ -1131,6 +1260,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_persistent_kernel(const __gri
     if (threadIdx.x < 16) reinterpret_cast<int *>(smem_raw + TRACE_COUNTS_OFFSET)[threadIdx.x] = 0;
     __syncthreads();
 #endif
+    build_sched(p, smem + OFF_SCHED, smem);  // the roles' tiles serve as scratch until it returns
     if (static_cast<int>(blockIdx.x) < p.C)
         cons::run(p, smem, blockIdx.x);
     else

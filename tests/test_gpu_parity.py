@@ -48,6 +48,20 @@ def test_small_cases(name):
     check_case(inp)
 
 
+def test_unequal_lengths_schedules():
+    """Sequences of unequal length go to consumers by the longest-first table
+    (up to 1024 chains) or, beyond that, by the plain stride order; both must
+    cover every chain exactly once. Lengths include empty and one-token
+    sequences; every head is checked against the oracle."""
+    rng = np.random.default_rng(7)
+    for n_seq, H in ((24, 8), (70, 16)):  # 192 chains (table), 1120 chains (stride order)
+        lens = [int(x) for x in rng.integers(0, 200, size=n_seq)]
+        lens[3], lens[5] = 0, 1
+        lens[7] = 700  # one long sequence
+        inp = kin.make_inputs(lens, H, seed=300 + n_seq, state_std=0.02)
+        check_case(inp)
+
+
 def test_tiny_workload():
     check_case(kin.make_workload(kin.workloads()["tiny_T256_H2"]))
 
