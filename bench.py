@@ -313,7 +313,7 @@ def bench_gpu(a, world, rank, local):
                                inp["lower_bound"], o, fs, None, stream)
         else:
             kda.kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], d["initial_state"],
-                              inp["scale"], inp["lower_bound"], o, fs, None, stream)
+                              inp["scale"], inp["lower_bound"], o, fs, None, stream, raw_gates=a.raw_gates)
 
     for _ in range(max(3, a.warmup)):
         flush.zero_()
@@ -390,7 +390,8 @@ def bench_gpu(a, world, rank, local):
             "warmup": a.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": (value / world / PAGES_HEADLINE_TOKENS_PER_S) if a.workload == DEFAULT_WORKLOAD else None,
             "dtype": ("fp32 (bf16 q, k, v)" if decode else "bf16/fp16 (fp32 accumulate, fp32 state and o)"),
-            "data": "synthetic", "config": workload_config(a.workload, inp),
+            "data": "synthetic", "config": dict(workload_config(a.workload, inp),
+                                                **({"gates": "raw, activated in the kernel"} if a.raw_gates else {})),
             "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": traffic,
                          "kernel": kernel, "algorithmic_bytes_per_launch": alg_bytes,
@@ -416,6 +417,8 @@ def main():
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
     p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--raw-gates", action="store_true",
+                   help="time kda_chunk_fwd_raw_gates (g and beta activated inside the kernel)")
     a = p.parse_args()
     if a.warmup < 3:
         a.warmup = 3

@@ -74,8 +74,8 @@ typedef enum {
  *   q, k          bf16 [total_tokens, num_heads, 128]; k is expected to be
  *                 L2-normalised per (token, head) as in the model (not checked).
  *   v             bf16 [total_tokens, num_heads, 128].
- *                 total_tokens may not exceed 2^31 - 65 (the tensor-copy
- *                 coordinates of the input loads are 32-bit).
+ *                 total_tokens may not exceed 2^31 - 65 (token offsets of the
+ *                 per-chunk tasks are 32-bit).
  *   g             fp32 [total_tokens, num_heads, 128]: natural-log decay per
  *                 key channel, already activated; lower_bound <= g <= 0.
  *   beta          fp32 [total_tokens, num_heads].
@@ -104,10 +104,9 @@ typedef enum {
  * Alignment: q, k, v, g, o, initial_state, final_state 16-byte aligned;
  *   beta, cu_seqlens, status_dev 4-byte aligned.
  * Precision: products run on tensor cores with fp32 accumulation. The Aqk
- *   strip operands are split into two bf16 terms (bf16's exponent range holds
- *   the 2^57.7 factors, the split keeps ~16 significant bits); the Akk strips
- *   use bf16; the solve, WY form, state recurrence and output products use
- *   fp16 operands. The state stays fp32 across the whole sequence. Inputs must
+ *   strip operands are tf32 (fp32's exponent range holds the 2^57.7 factors,
+ *   with 11 significant bits); the Akk strips use bf16; the solve, WY form,
+ *   state recurrence and output products use fp16 operands. The state stays fp32 across the whole sequence. Inputs must
  *   keep |v|, |initial_state| and the state below ~6e4 (fp16 operand range);
  *   otherwise KDA_ERR_VALUE_RANGE is reported.
  *   workspace     device scratch of at least kda_chunk_fwd_workspace_size(num_seqs,
@@ -129,6 +128,33 @@ kda_status_t kda_chunk_fwd(const void *q, const void *k, const void *v, const fl
                            float lower_bound, float *o, float *final_state,
                            int32_t *status_dev, void *workspace, size_t workspace_bytes,
                            kda_stream_t stream);
+
+/*
+ * kda_chunk_fwd_raw_gates — kda_chunk_fwd taking the gate and beta before their
+ * activations, which run inside the kernel on the tiles it has loaded: the
+ * fusion of "在 TPU 上加速 Kimi K3 KDA" §6.1 (activate_gate(g, A_log[head],
+ * dt_bias[head]) moves into the intra-chunk kernel ahead of the chunk prefix
+ * sum) and of the fused beta sigmoid in the Kimi K3 PP16 prefill notes' flag
+ * table. The pages name the gate activation without defining it; this library
+ * reads it as
+ *     g    = lower_bound * sigmoid(exp(A_log[h]) * (g_raw + dt_bias[h][c]))
+ *     beta = sigmoid(beta_raw)
+ * which keeps lower_bound <= g <= 0 by construction and, with A_log = 0 and
+ * dt_bias = 0, is the g = lower_bound * sigmoid(x) form of the synthetic inputs.
+ *   g_raw     fp32 [total_tokens, num_heads, 128], 16-byte aligned
+ *   beta_raw  fp32 [total_tokens, num_heads], 4-byte aligned
+ *   A_log     fp32 [num_heads], or NULL for zeros
+ *   dt_bias   fp32 [num_heads, 128], 16-byte aligned, or NULL for zeros
+ * Every other argument, output, limit and error is as for kda_chunk_fwd
+ * (KDA_ERR_GATE_RANGE then flags only non-finite activated gates).
+ */
+kda_status_t kda_chunk_fwd_raw_gates(const void *q, const void *k, const void *v, const float *g_raw,
+                                     const float *beta_raw, const float *A_log, const float *dt_bias,
+                                     const int32_t *cu_seqlens, int32_t num_seqs, int64_t total_tokens,
+                                     int32_t num_heads, int32_t head_dim_k, int32_t head_dim_v,
+                                     const float *initial_state, float scale, float lower_bound, float *o,
+                                     float *final_state, int32_t *status_dev, void *workspace,
+                                     size_t workspace_bytes, kda_stream_t stream);
 
 /* Workspace bytes kda_chunk_fwd needs for these sizes on the current device
  * (0 when num_seqs or num_heads is 0, or no usable device is current). */

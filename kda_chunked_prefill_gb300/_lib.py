@@ -29,8 +29,8 @@ KDA_DEBUG_WITHHOLD_READY = 1
 
 HEAD_DIM = 128
 EXPORTED = ("kda_chunk_fwd", "kda_chunk_fwd_workspace_size", "kda_chunk_fwd_static_scratch",
-            "kda_chunk_fwd_debug", "kda_decode_fwd", "kda_chunk_fwd_launches", "kda_status_string",
-            "kda_version")
+            "kda_chunk_fwd_debug", "kda_chunk_fwd_raw_gates", "kda_decode_fwd", "kda_chunk_fwd_launches",
+            "kda_status_string", "kda_version")
 DECODE_MAX_TOKENS = 64
 
 _lock = threading.Lock()
@@ -65,6 +65,9 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.kda_chunk_fwd.restype = ctypes.c_int
         lib.kda_chunk_fwd_debug.argtypes = lib.kda_chunk_fwd.argtypes + [ctypes.c_uint32]
         lib.kda_chunk_fwd_debug.restype = ctypes.c_int
+        lib.kda_chunk_fwd_raw_gates.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i64, i32, i32, i32, vp, f32, f32,
+                                                vp, vp, vp, vp, ctypes.c_size_t, vp]
+        lib.kda_chunk_fwd_raw_gates.restype = ctypes.c_int
         lib.kda_decode_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, f32, f32, vp, vp, vp, vp]
         lib.kda_decode_fwd.restype = ctypes.c_int
         lib.kda_chunk_fwd_workspace_size.argtypes = [i32, i32]
@@ -127,7 +130,8 @@ def _check(t, name, dtype, shape, device):
 
 
 def kda_chunk_fwd(q, k, v, g, beta, cu_seqlens, initial_state, scale: float, lower_bound: float,
-                  o, final_state, status=None, stream=None, workspace=None, debug_flags: int = 0) -> int:
+                  o, final_state, status=None, stream=None, workspace=None, debug_flags: int = 0,
+                  raw_gates: bool = False, A_log=None, dt_bias=None) -> int:
     """Call the C entry point ``kda_chunk_fwd`` with caller-allocated outputs.
 
     q, k, v: bf16 [T,H,128]; o: fp32 [T,H,128]; g: fp32 [T,H,128]; beta: fp32 [T,H];
@@ -137,7 +141,10 @@ def kda_chunk_fwd(q, k, v, g, beta, cu_seqlens, initial_state, scale: float, low
     one CUDA device. ``stream`` is a ``torch.cuda.Stream`` (default: the current
     stream). Raises ``KdaError`` on a host-side error; returns ``KDA_OK`` once
     the work is queued. A nonzero ``debug_flags`` calls ``kda_chunk_fwd_debug``
-    (failure-detection testing; see include/kda.h).
+    (failure-detection testing; see include/kda.h). ``raw_gates=True`` calls
+    ``kda_chunk_fwd_raw_gates``: ``g`` and ``beta`` are then the raw gate and
+    beta projections, activated inside the kernel with the optional per-head
+    ``A_log`` (fp32 [H]) and ``dt_bias`` (fp32 [H,128]).
     """
     T, H, D = q.shape
     N = cu_seqlens.shape[0] - 1
@@ -157,6 +164,12 @@ def kda_chunk_fwd(q, k, v, g, beta, cu_seqlens, initial_state, scale: float, low
         _check(final_state, "final_state", torch.float32, (N, H, D, v.shape[2]), dev)
     if status is not None:
         _check(status, "status", torch.int32, (1,), dev)
+    if not raw_gates and (A_log is not None or dt_bias is not None):
+        raise ValueError("A_log and dt_bias apply only with raw_gates=True")
+    if A_log is not None:
+        _check(A_log, "A_log", torch.float32, (H,), dev)
+    if dt_bias is not None:
+        _check(dt_bias, "dt_bias", torch.float32, (H, D), dev)
     if stream is None:
         stream = torch.cuda.current_stream(dev)
     if workspace is None:
@@ -167,20 +180,28 @@ def kda_chunk_fwd(q, k, v, g, beta, cu_seqlens, initial_state, scale: float, low
             _ptr(initial_state), float(scale), float(lower_bound), _ptr(o), _ptr(final_state),
             _ptr(status), _ptr(workspace), workspace.numel(), ctypes.c_void_p(stream.cuda_stream))
     lib = load_library()
-    rc = lib.kda_chunk_fwd_debug(*args, int(debug_flags)) if debug_flags else lib.kda_chunk_fwd(*args)
+    if raw_gates:
+        if debug_flags:
+            raise ValueError("debug_flags and raw_gates cannot be combined")
+        rc = lib.kda_chunk_fwd_raw_gates(*args[:5], _ptr(A_log), _ptr(dt_bias), *args[5:])
+        what = "kda_chunk_fwd_raw_gates"
+    else:
+        rc = lib.kda_chunk_fwd_debug(*args, int(debug_flags)) if debug_flags else lib.kda_chunk_fwd(*args)
+        what = "kda_chunk_fwd"
     if rc != KDA_OK:
-        raise KdaError(rc, "kda_chunk_fwd")
+        raise KdaError(rc, what)
     return rc
 
 
 def chunk_fwd(q, k, v, g, beta, cu_seqlens, initial_state=None, scale: Optional[float] = None,
               lower_bound: float = -5.0, output_final_state: bool = True, check: bool = False,
-              stream=None):
+              stream=None, raw_gates: bool = False, A_log=None, dt_bias=None):
     """Allocate ``o`` (and ``final_state``) and run ``kda_chunk_fwd``.
 
     Returns ``(o, final_state)``; ``final_state`` is None when not requested.
     With ``check=True`` the device status word is read back (a synchronising
-    copy) and a device-detected error raises ``KdaError``.
+    copy) and a device-detected error raises ``KdaError``. ``raw_gates``,
+    ``A_log`` and ``dt_bias`` are passed to ``kda_chunk_fwd``.
     """
     T, H, D = q.shape
     N = cu_seqlens.shape[0] - 1
@@ -190,7 +211,8 @@ def chunk_fwd(q, k, v, g, beta, cu_seqlens, initial_state=None, scale: Optional[
     fs = (torch.empty((N, H, D, v.shape[2]), dtype=torch.float32, device=q.device)
           if output_final_state else None)
     status = torch.zeros(1, dtype=torch.int32, device=q.device) if check else None
-    kda_chunk_fwd(q, k, v, g, beta, cu_seqlens, initial_state, scale, lower_bound, o, fs, status, stream)
+    kda_chunk_fwd(q, k, v, g, beta, cu_seqlens, initial_state, scale, lower_bound, o, fs, status, stream,
+                  raw_gates=raw_gates, A_log=A_log, dt_bias=dt_bias)
     if check:
         code = int(status.item())
         if code != KDA_OK:

@@ -25,13 +25,14 @@ kda_status_t fwd_impl(const void *q, const void *k, const void *v, const float *
                       const int32_t *cu_seqlens, int32_t num_seqs, int64_t total_tokens, int32_t num_heads,
                       int32_t head_dim_k, int32_t head_dim_v, const float *initial_state, float scale,
                       float lower_bound, float *o, float *final_state, int32_t *status_dev, void *workspace,
-                      size_t workspace_bytes, kda_stream_t stream, uint32_t debug_flags) {
+                      size_t workspace_bytes, kda_stream_t stream, uint32_t debug_flags, bool raw = false,
+                      const float *A_log = nullptr, const float *dt_bias = nullptr) {
     if (head_dim_k != KDA_HEAD_DIM || head_dim_v != KDA_HEAD_DIM) return KDA_ERR_UNSUPPORTED;
     if (num_seqs < 0 || total_tokens < 0 || num_heads < 1) return KDA_ERR_INVALID_ARG;
     if (static_cast<int64_t>(num_seqs) * num_heads > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
     if (total_tokens > (int64_t{1} << 40) / (static_cast<int64_t>(num_heads) * KDA_HEAD_DIM))
         return KDA_ERR_INVALID_ARG;
-    if (total_tokens > kKdaMaxTokens) return KDA_ERR_UNSUPPORTED;  // tensor-copy coordinates are 32-bit
+    if (total_tokens > kKdaMaxTokens) return KDA_ERR_UNSUPPORTED;  // task token offsets are 32-bit
     if (!(scale == scale) || !lower_bound_ok(lower_bound)) return KDA_ERR_INVALID_ARG;
     if (num_seqs == 0) return total_tokens == 0 ? KDA_OK : KDA_ERR_INVALID_ARG;
     if (!cu_seqlens || !aligned(cu_seqlens, 4)) return KDA_ERR_INVALID_ARG;
@@ -42,7 +43,7 @@ kda_status_t fwd_impl(const void *q, const void *k, const void *v, const float *
             return KDA_ERR_INVALID_ARG;
     }
     if ((initial_state && !aligned(initial_state, 16)) || (final_state && !aligned(final_state, 16)) ||
-        (status_dev && !aligned(status_dev, 4)))
+        (status_dev && !aligned(status_dev, 4)) || (A_log && !aligned(A_log, 4)) || (dt_bias && !aligned(dt_bias, 16)))
         return KDA_ERR_INVALID_ARG;
     if (!workspace || !aligned(workspace, 16)) return KDA_ERR_INVALID_ARG;
     const size_t need = kda::pers::workspace_bytes(static_cast<int64_t>(num_seqs) * num_heads);
@@ -72,6 +73,9 @@ kda_status_t fwd_impl(const void *q, const void *k, const void *v, const float *
     p.C = 0;
     p.debug = debug_flags;
     p.spin = 0;
+    p.raw = raw ? 1 : 0;
+    p.A_log = A_log;
+    p.dt_bias = dt_bias;
     const cudaError_t e = kda::pers::launch(p, workspace_bytes, s);
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
@@ -102,6 +106,18 @@ kda_status_t kda_chunk_fwd_debug(const void *q, const void *k, const void *v, co
     return fwd_impl(q, k, v, g, beta, cu_seqlens, num_seqs, total_tokens, num_heads, head_dim_k, head_dim_v,
                     initial_state, scale, lower_bound, o, final_state, status_dev, workspace, workspace_bytes,
                     stream, debug_flags);
+}
+
+kda_status_t kda_chunk_fwd_raw_gates(const void *q, const void *k, const void *v, const float *g_raw,
+                                     const float *beta_raw, const float *A_log, const float *dt_bias,
+                                     const int32_t *cu_seqlens, int32_t num_seqs, int64_t total_tokens,
+                                     int32_t num_heads, int32_t head_dim_k, int32_t head_dim_v,
+                                     const float *initial_state, float scale, float lower_bound, float *o,
+                                     float *final_state, int32_t *status_dev, void *workspace,
+                                     size_t workspace_bytes, kda_stream_t stream) {
+    return fwd_impl(q, k, v, g_raw, beta_raw, cu_seqlens, num_seqs, total_tokens, num_heads, head_dim_k,
+                    head_dim_v, initial_state, scale, lower_bound, o, final_state, status_dev, workspace,
+                    workspace_bytes, stream, 0u, true, A_log, dt_bias);
 }
 
 size_t kda_chunk_fwd_workspace_size(int32_t num_seqs, int32_t num_heads) {

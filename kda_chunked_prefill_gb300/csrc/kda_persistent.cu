@@ -368,7 +368,9 @@ constexpr int OFF_T = OFF_LD + 4352;          // T = (I+L)^-1, fp16 [64][RSA] (l
 constexpr int OFF_TAB = OFF_T + SZ_A;         // per-channel tables, fp32 [20][128]
 constexpr int OFF_BETA = OFF_TAB + 10240;
 constexpr int OFF_MISC = OFF_BETA + 256;      // flags and the task broadcast (32 ints)
-constexpr int SMEM = OFF_MISC + 128;
+constexpr int OFF_GPAR = OFF_MISC + 128;      // raw gates: the task head's dt_bias row (128 fp32) and A_log
+constexpr int SMEM = OFF_GPAR + 528;
+static_assert(OFF_GPAR % 16 == 0, "cp.async destinations are 16-byte aligned");
 // Warp w runs on sub-partition w % 4. During the strips, warps 0-9 hold the
 // ten tiles (three on partitions 0 and 1, two on 2 and 3); the diagonal
 // inverses run on warps 10, 11, 14, 15 (partitions 2 and 3) and the ring work,
@@ -476,6 +478,12 @@ __device__ __forceinline__ void issue_loads(const Params &p, unsigned char *smem
         cp_async16(smem + OFF_GKB + g_chunk(r, c4), p.g + static_cast<size_t>(tk.t0 + (ok ? r : 0)) * rs + hb + c4,
                    ok ? 16 : 0);
     }
+    if (p.raw && tid < 33) {  // the gate activation's per-head parameters (zeros when not given)
+        if (tid < 32)
+            cp_async16(smem + OFF_GPAR + 16 * tid, p.dt_bias ? p.dt_bias + hb + 4 * tid : p.g, p.dt_bias ? 16 : 0);
+        else
+            cp_async4(smem + OFF_GPAR + 512, p.A_log ? p.A_log + tk.h : p.g, p.A_log ? 4 : 0);
+    }
     cp_async_commit();
 #pragma unroll
     for (int it = 0; it < BT * 16 / NCOMP; ++it) {  // q, k, v: 64 rows x 16 chunks of 8 channels
@@ -531,6 +539,13 @@ __device__ __forceinline__ bool run_task(const Params &p, const Ring &Rg, unsign
         float x[16];
 #pragma unroll
         for (int q = 0; q < 16; ++q) x[q] = *reinterpret_cast<const float *>(sGb + g_elem(16 * rq + q, chn));
+        if (p.raw) {  // g = lower_bound * sigmoid(e^A_log (g_raw + dt_bias)); rows past the sequence end stay 0
+            const float *gp = reinterpret_cast<const float *>(smem + OFF_GPAR);
+            const float a = __expf(gp[128]), db = gp[chn];
+#pragma unroll
+            for (int q = 0; q < 16; ++q)
+                x[q] = (16 * rq + q < cur.nv) ? __fdividef(p.lb, 1.f + __expf(-a * (x[q] + db))) : 0.f;
+        }
         float acc = 0.f;
         bool gb = false;
 #pragma unroll
@@ -570,6 +585,10 @@ __device__ __forceinline__ bool run_task(const Params &p, const Ring &Rg, unsign
     if (tid == REL_TID) bulk_wait_read();  // the previous image has been read out and may be rewritten
     cp_async_wait_all();  // q, k, v and beta
     sync_compute();
+    if (p.raw) {  // beta = sigmoid(beta_raw); rows past the sequence end stay 0
+        if (tid < BT) sBeta[tid] = tid < cur.nv ? __fdividef(1.f, 1.f + __expf(-sBeta[tid])) : 0.f;
+        sync_compute();
+    }
     KDA_TRACE_EV(p, 21, 0);
 
     // ---- steps 2a/4a: elementwise operands; q_hat, kg, beta*v and

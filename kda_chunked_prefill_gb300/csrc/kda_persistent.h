@@ -26,6 +26,9 @@ struct Params {
     int32_t C;           // consumer CTAs (set by launch)
     int32_t Cws;         // consumers the workspace rings were sized for (>= C)
     uint32_t debug;      // KDA_DEBUG_* flags (0 in normal calls)
+    int32_t raw;         // 1: g and beta are raw (activated in the producer), see kda_chunk_fwd_raw_gates
+    const float *A_log;  // [H] or NULL (raw mode)
+    const float *dt_bias;  // [H][128] or NULL (raw mode)
     long long spin;      // polls before a wait gives up
 };
 

@@ -11,6 +11,9 @@ Contents
 ``kda_recurrence``  the oracle proper: the token-by-token fp64 recurrence of
                     Kimi Delta Attention, compiled from ``kda_oracle.c`` and
                     run on host threads over (sequence, head) chains.
+``gates``           the gate and beta activations of the raw-gate entry point
+                    (a stated reading: the pages name the gate activation
+                    without defining it).
 ``chunked``         a second, independent fp64 formulation — the chunked
                     algebra of the TPU report (§4 strip GEMMs with sub-block
                     midpoints, the Neumann factor chain, the WY form and the

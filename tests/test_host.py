@@ -108,6 +108,30 @@ def test_debug_entry_validates_like_the_plain_call(lib):
                        beta=None, o=None, cu=None) == kda.KDA_OK
 
 
+def _call_raw(lib, **over):
+    fake = ctypes.c_void_p(0x10000)
+    args = dict(q=fake, k=fake, v=fake, g=fake, beta=fake, A=None, dt=None, cu=fake, N=2, T=100, H=4, dk=128,
+                dv=128, s0=None, scale=0.088, lb=-5.0, o=fake, sT=None, status=None, ws=fake, wsb=1 << 20,
+                stream=None)
+    args.update(over)
+    return lib.kda_chunk_fwd_raw_gates(args["q"], args["k"], args["v"], args["g"], args["beta"], args["A"],
+                                       args["dt"], args["cu"], args["N"], args["T"], args["H"], args["dk"],
+                                       args["dv"], args["s0"], args["scale"], args["lb"], args["o"], args["sT"],
+                                       args["status"], args["ws"], args["wsb"], args["stream"])
+
+
+@pytest.mark.parametrize("over,code", [
+    ({"dk": 64}, kda.KDA_ERR_UNSUPPORTED),
+    ({"g": None}, kda.KDA_ERR_INVALID_ARG),
+    ({"lb": -20.0}, kda.KDA_ERR_INVALID_ARG),
+    ({"dt": ctypes.c_void_p(0x10008)}, kda.KDA_ERR_INVALID_ARG),  # dt_bias not 16-byte aligned
+    ({"A": ctypes.c_void_p(0x10002)}, kda.KDA_ERR_INVALID_ARG),   # A_log not 4-byte aligned
+    ({"N": 0, "T": 0, "q": None, "k": None, "v": None, "g": None, "beta": None, "o": None}, kda.KDA_OK),
+])
+def test_raw_gate_entry_validates_like_the_plain_call(lib, over, code):
+    assert _call_raw(lib, **over) == code
+
+
 def _call_decode(lib, **over):
     fake = ctypes.c_void_p(0x10000)
     args = dict(q=fake, k=fake, v=fake, g=fake, beta=fake, N=4, Tn=1, H=4, dk=128, dv=128, s0=None,

@@ -337,3 +337,39 @@ def test_pins_reject_planted_mistakes(kind):
     ref, _ = basis_key_closed_form(qb, ch, vb, gb, bb, 1.0)
     bad2 = not np.allclose(ob, ref, atol=1e-9)
     assert bad1 or bad2
+
+
+# ---- gate and beta activations (the raw-gate entry point; a stated reading)
+def test_gate_activation_closed_forms():
+    """The restated activation against closed forms of the logistic function:
+    sigma(0) = 1/2, sigma(ln 3) = 3/4, sigma(x) + sigma(-x) = 1, the limits, and
+    the per-head scale e^A_log and per-channel shift dt_bias entering as
+    e^A_log * (x + dt_bias)."""
+    from oracle import gates
+    lb = -5.0
+    x = np.zeros((2, 3, 4))
+    assert np.allclose(gates.activate_gate(x, lb), lb / 2, rtol=0, atol=0)
+    assert abs(gates.sigmoid(math.log(3.0)) - 0.75) < 1e-15
+    r = np.random.default_rng(0).normal(size=(5, 2, 4)) * 4
+    assert np.allclose(gates.activate_gate(r, lb) + gates.activate_gate(-r, lb), lb, atol=1e-13)
+    big = np.full((1, 1, 2), 800.0)
+    assert np.all(gates.activate_gate(big, lb) == lb) and np.all(gates.activate_gate(-big, lb) == 0.0)
+    g = gates.activate_gate(r, lb)
+    assert np.all((g >= lb) & (g <= 0))
+    # e^A_log = 2 doubles the argument; dt_bias = -x brings it back to sigma(0)
+    A = np.array([math.log(2.0), 0.0])
+    dt = np.zeros((2, 4))
+    g2 = gates.activate_gate(r, lb, A_log=A, dt_bias=dt)
+    assert np.allclose(g2[:, 0], lb * (1 / (1 + np.exp(-2 * r[:, 0]))), atol=1e-13)
+    assert np.allclose(g2[:, 1], g[:, 1], atol=0)
+    shift = gates.activate_gate(r, lb, dt_bias=-r[0])
+    assert np.allclose(shift[0], lb / 2, atol=1e-15)
+
+
+def test_beta_activation_closed_forms():
+    from oracle import gates
+    assert gates.activate_beta(np.zeros(3)).tolist() == [0.5, 0.5, 0.5]
+    x = np.linspace(-30, 30, 61)
+    b = gates.activate_beta(x)
+    assert np.all((b > 0) & (b < 1)) and np.all(np.diff(b) > 0)
+    assert np.allclose(b + gates.activate_beta(-x), 1.0, atol=1e-15)
