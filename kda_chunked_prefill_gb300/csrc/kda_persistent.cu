@@ -182,7 +182,8 @@ __device__ __forceinline__ int chain_info(const Params &p, const int32_t *cu, in
 // ------------------------------------------------------------ chain schedule
 // Which chains each consumer runs, in order. When every sequence has the same
 // number of chunks, consumer k takes chains k, k + C, k + 2C, ... (no table).
-// Otherwise, for at most SCHED_MAX_CHAINS chains, every CTA builds the same
+// Otherwise, for at most SCHED_MAX_CHAINS chains and when its cost (about
+// 150 ns per sequence) is small against the run, every CTA builds the same
 // table at start-up (deterministically, in shared memory): sequences in
 // decreasing order of their chunk count hand their H chains to the H consumers
 // with the least work so far (ties to the lower index), the longest-first
@@ -233,6 +234,7 @@ __device__ void build_sched(const Params &p, unsigned char *sched, unsigned char
     if (tid < 32) {
         bool uneq = false;
         int first = 0;
+        long long chunks = 0;  // chunks of all sequences (one head)
         for (int n0 = 0; n0 <= N; n0 += 32) {
             const int n = n0 + tid;
             int32_t b = 0, e = 0;
@@ -245,9 +247,16 @@ __device__ void build_sched(const Params &p, unsigned char *sched, unsigned char
             if (n0 == 0) first = __shfl_sync(0xffffffffu, nc, 0);
             if (fits && n < N) nchk[n] = nc;
             uneq |= __any_sync(0xffffffffu, n < N && nc != first);
+            chunks += nc;
         }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) chunks += __shfl_xor_sync(0xffffffffu, chunks, o);
+        // the table costs about 150 ns per sequence in every CTA; build it only
+        // when that is under 2 % of the producers' expected time (~7 us per chunk)
+        const long long prod_ns = chunks * H * 7000 / (static_cast<int>(gridDim.x) - C > 0 ? static_cast<int>(gridDim.x) - C : 1);
+        const bool worth = N <= 256 && static_cast<long long>(N) * 150 * 50 <= prod_ns;
         if (tid == 0) {
-            flag[0] = (fits && uneq) ? 1 : 0;
+            flag[0] = (fits && uneq && worth) ? 1 : 0;
             flag[1] = cache_cu ? 1 : 0;
         }
     }

@@ -54,10 +54,12 @@ def test_unequal_lengths_schedules():
     cover every chain exactly once. Lengths include empty and one-token
     sequences; every head is checked against the oracle."""
     rng = np.random.default_rng(7)
-    for n_seq, H in ((24, 8), (70, 16)):  # 192 chains (table), 1120 chains (stride order)
-        lens = [int(x) for x in rng.integers(0, 200, size=n_seq)]
+    # 16 sequences of ~3000 tokens, H = 4: 64 chains, long enough for the table
+    # to pay for itself; 70 short sequences, H = 16: 1120 chains (stride order)
+    for n_seq, H, lo, hi in ((16, 4, 500, 5000), (70, 16, 0, 200)):
+        lens = [int(x) for x in rng.integers(lo, hi, size=n_seq)]
         lens[3], lens[5] = 0, 1
-        lens[7] = 700  # one long sequence
+        lens[7] = 7000  # one long sequence
         inp = kin.make_inputs(lens, H, seed=300 + n_seq, state_std=0.02)
         check_case(inp)
 
