@@ -1093,12 +1093,14 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
             if (tid == 0) {
                 const bool was_alive = misc[0] != 0;  // then slot j's copy has been issued
                 if (was_alive && wait_mbar(R, &full[b], (j >> 1) & 1, p.status)) {
-                    fence_proxy_async_global();
-                    st_release(&R.freed[k * RING + j % RING], j + 1);
+                    // the copy of slot j has completed (its reads are done): free the
+                    // slot without ordering this thread's pending o stores before it
+                    st_relaxed(&R.freed[k * RING + j % RING], j + 1);
                     issued_next = false;
                     if (j + 1 < total && ld_acquire(&R.ready[k * RING + (j + 1) % RING]) >= j + 2) {
                         issue(j + 1);
                         issued_next = true;
+                        KDA_TRACE_ANY(p, 17, j + 1);
                     }
                 } else {
                     if (was_alive) drain_mbar(&full[b], (j >> 1) & 1);  // let it land before leaving
@@ -1239,8 +1241,10 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
                     *reinterpret_cast<const float4 *>(stg + rr * OST + 4 * lane);
             KDA_TRACE_EV(p, 12, j);
             if (tid == 0 && !issued_next && j + 1 < total) {
-                if (wait_flag_geq(R, &R.ready[k * RING + (j + 1) % RING], j + 2, p.status))
+                if (wait_flag_geq(R, &R.ready[k * RING + (j + 1) % RING], j + 2, p.status)) {
                     issue(j + 1);
+                    KDA_TRACE_ANY(p, 18, j + 1);
+                }
                 else
                     misc[0] = 0;
             }
