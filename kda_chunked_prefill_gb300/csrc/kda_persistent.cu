@@ -1036,9 +1036,7 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
         unsigned char *dst = smem + ((jj & 1) ? OFF_BUF1 : OFF_BUF0);
         fence_proxy_async_global();
         mbar_arrive_expect_tx(&full[jj & 1], SLOT_BYTES);
-        bulk_g2s(dst, src, 32768, &full[jj & 1]);
-        bulk_g2s(dst + 32768, src + 32768, 32768, &full[jj & 1]);
-        bulk_g2s(dst + 65536, src + 65536, SLOT_BYTES - 65536, &full[jj & 1]);
+        bulk_g2s(dst, src, SLOT_BYTES, &full[jj & 1]);
     };
     bool issued_next = false;  // thread 0 only
     if (tid == 0 && total > 0) {
