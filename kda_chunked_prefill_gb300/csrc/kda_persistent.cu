@@ -357,6 +357,12 @@ __device__ __forceinline__ bool map_task(const Params &p, const unsigned char *s
 // bulk store; while warps 0-9 compute the strips, one thread of the idle last
 // warp publishes the previous slot, draws the next task and waits for this
 // task's slot to be free, so none of that memory traffic stalls the warps.
+// Round an fp32 value to tf32 (nearest, ties away from zero) for a tf32 MMA
+// operand: adding half a tf32 unit in the last place to the sign-magnitude bit
+// pattern carries into bit 13 exactly when the dropped 13 bits are at least
+// half of it, and the MMA reads only the upper 19 bits. Finite inputs only.
+__device__ __forceinline__ uint32_t tf32_rna(float x) { return __float_as_uint(x) + 0x1000u; }
+
 namespace prod {
 // q, k, v and their derived tiles are [64 tokens][128 channels] 16-bit tiles
 // and g is a [64][128] fp32 tile, all in the 128-byte-swizzled layout the
@@ -662,8 +668,8 @@ __device__ __forceinline__ bool run_task(const Params &p, const Ring &Rg, unsign
                     res[e][5] = kk * b * EL[ce];   // k e^(G_last - G)
                     kb[ce] = kk * b;               // k e^(G_m - G)
                 }
-                oQa[2 * q2] = to_tf32(res[0][0]);
-                oQa[2 * q2 + 1] = to_tf32(res[1][0]);
+                oQa[2 * q2] = tf32_rna(res[0][0]);
+                oQa[2 * q2 + 1] = tf32_rna(res[1][0]);
                 oKa[q2] = pack_bf16(res[0][1], res[1][1]);
                 range_bad |= !(f16_ok(res[0][2]) && f16_ok(res[1][2]));
                 oBv[q2] = pack_f16(res[0][2], res[1][2]);
@@ -759,8 +765,8 @@ __device__ __forceinline__ bool run_task(const Params &p, const Ring &Rg, unsign
                 const float2 x0 = *reinterpret_cast<const float2 *>(row + c0);
                 const float2 x1 = *reinterpret_cast<const float2 *>(row + c0 + 8);
                 const float b00 = x0.x * f0.x, b01 = x0.y * f0.y, b10 = x1.x * f1.x, b11 = x1.y * f1.y;
-                mma1688_tf32(aq[nt], fa0, to_tf32(b00), to_tf32(b01));
-                mma1688_tf32(aq[nt], fa1, to_tf32(b10), to_tf32(b11));
+                mma1688_tf32(aq[nt], fa0, tf32_rna(b00), tf32_rna(b01));
+                mma1688_tf32(aq[nt], fa1, tf32_rna(b10), tf32_rna(b11));
                 mma16816(ak[nt], fk, pack_bf16(b00, b01), pack_bf16(b10, b11));
             }
         }
