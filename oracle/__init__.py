@@ -14,6 +14,9 @@ Contents
 ``gates``           the gate and beta activations of the raw-gate entry point
                     (a stated reading: the pages name the gate activation
                     without defining it).
+``norm``            the gated RMSNorm of the output for the fused-norm entry
+                    point (a stated reading: the pages name the operation
+                    without writing it out).
 ``chunked``         a second, independent fp64 formulation — the chunked
                     algebra of the TPU report (§4 strip GEMMs with sub-block
                     midpoints, the Neumann factor chain, the WY form and the

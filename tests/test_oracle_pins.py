@@ -373,3 +373,75 @@ def test_beta_activation_closed_forms():
     b = gates.activate_beta(x)
     assert np.all((b > 0) & (b < 1)) and np.all(np.diff(b) > 0)
     assert np.allclose(b + gates.activate_beta(-x), 1.0, atol=1e-15)
+
+
+
+def _gated_norm_pins(fn):
+    """The gated-RMSNorm pins, worked by hand, as a list of the ones `fn`
+    (o, gate, weight, eps) -> y fails (an exception counts as failing): the
+    mean (not the sum) of squares over the value channels of one (token, head)
+    row, eps inside the square root, the weight on the channel axis, and a
+    sigmoid (not a swish) gate."""
+    big = lambda shape: np.full(shape, 800.0)  # sigmoid(800) == 1 in fp64
+    r = np.random.default_rng(1).normal(size=(4, 3, 8)) * np.array([1e-3, 1.0, 50.0])[None, :, None]
+    o = np.random.default_rng(2).normal(size=(2, 3, 3))
+    w = np.array([1.0, 2.0, -3.0])
+
+    def unit(eps=0.0):
+        return fn(r, big(r.shape), np.ones(8), eps)
+
+    def eps_case():
+        y = fn(np.array([[[1e-3, 1e-3], [0.0, 0.0]]]), big((1, 2, 2)), np.ones(2), 1e-6)
+        return np.allclose(y[0, 0], 1e-3 / math.sqrt(2e-6), rtol=1e-14) and np.all(y[0, 1] == 0.0)
+
+    pins = {
+        "worked example [3, 4]": lambda: np.allclose(fn(np.array([[[3.0, 4.0]]]), big((1, 1, 2)), np.ones(2), 0.0),
+                                                     [[[3 / math.sqrt(12.5), 4 / math.sqrt(12.5)]]], rtol=1e-15, atol=0),
+        # every row normalised on its own: unit RMS whatever the row's scale
+        "unit RMS per row": lambda: np.allclose(np.sqrt(np.mean(unit() ** 2, axis=-1)), 1.0, atol=1e-14),
+        "scale invariance": lambda: np.allclose(fn(7.5 * r, big(r.shape), np.ones(8), 0.0), unit(), atol=1e-14),
+        # gate 0 halves the output, gate ln 3 keeps three quarters
+        "sigmoid gate": lambda: (np.allclose(fn(r, np.zeros(r.shape), np.ones(8), 0.0), 0.5 * unit(), atol=1e-15)
+                                 and np.allclose(fn(r, np.full(r.shape, math.log(3.0)), np.ones(8), 0.0),
+                                                 0.75 * unit(), atol=1e-14)),
+        # the weight scales value channel c (V == H here, so a head-axis weight still broadcasts)
+        "weight on channels": lambda: np.allclose(fn(o, big(o.shape), w, 1e-6),
+                                                  fn(o, big(o.shape), np.ones(3), 1e-6) * w[None, None, :], atol=1e-15),
+        # eps inside the root: [1e-3, 1e-3] with eps 1e-6 gives 1e-3 / sqrt(2e-6); an all-zero row stays 0
+        "eps inside the root": eps_case,
+    }
+    bad = []
+    for name, check in pins.items():
+        try:
+            good = bool(check())
+        except (ValueError, IndexError):
+            good = False
+        if not good:
+            bad.append(name)
+    return bad
+
+
+def test_gated_rmsnorm_closed_forms():
+    from oracle import norm
+    assert _gated_norm_pins(norm.gated_rmsnorm) == []
+
+
+def _mutant_norm(kind):
+    """A deliberately wrong gated RMSNorm, one mistake per kind, used only to
+    show that the pins above reject it."""
+    from oracle import gates
+
+    def fn(o, gate, weight, eps):
+        o, gate, weight = (np.asarray(x, dtype=np.float64) for x in (o, gate, weight))
+        axis = 1 if kind == "norm_over_heads" else -1
+        ms = np.sum(o * o, axis=-1, keepdims=True) if kind == "sum" else np.mean(o * o, axis=axis, keepdims=True)
+        n = o / (np.sqrt(ms) + eps) if kind == "eps_outside" else o / np.sqrt(ms + eps)
+        gg = gate * gates.sigmoid(gate) if kind == "swish" else gates.sigmoid(gate)
+        ww = weight[None, :, None] if kind == "weight_on_heads" else weight
+        return n * ww * gg
+    return fn
+
+
+@pytest.mark.parametrize("kind", ["sum", "eps_outside", "swish", "weight_on_heads", "norm_over_heads"])
+def test_norm_pins_reject_planted_mistakes(kind):
+    assert _gated_norm_pins(_mutant_norm(kind)) != []
