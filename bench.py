@@ -49,6 +49,9 @@ STATE_BYTES = 128 * 128 * 4
 FLUSH_BYTES = 256 << 20
 
 
+NORM_GATE_BYTES_PER_TOKEN_HEAD = 256  # the bf16 output gate read by the fused gated RMSNorm
+
+
 def algorithmic_bytes(T, N, H, with_initial_state, with_final_state=True):
     return T * H * BYTES_PER_TOKEN_HEAD + N * H * STATE_BYTES * (int(with_initial_state) + int(with_final_state))
 
@@ -303,6 +306,12 @@ def bench_gpu(a, world, rank, local):
          ("q", "k", "v", "g", "beta", "cu_seqlens", "initial_state")}
     o = torch.empty(d["v"].shape, dtype=torch.float32, device=d["v"].device)
     fs = torch.empty((N, H, D, D), dtype=torch.float32, device=dev)
+    norm_kw = {}
+    if a.gated_norm:  # the output gate and weight of the fused gated RMSNorm of o
+        nrm = kin.make_norm_inputs(T, H, seed=wl.seed + 1000)
+        inp["norm_gate"] = nrm["gate"]
+        d["norm_gate"] = nrm["gate"].to(dev)
+        norm_kw = dict(norm_gate=d["norm_gate"], norm_weight=nrm["weight"].to(dev), norm_eps=nrm["eps"])
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     decode = wl.kind == "decode"
@@ -313,7 +322,8 @@ def bench_gpu(a, world, rank, local):
                                inp["lower_bound"], o, fs, None, stream)
         else:
             kda.kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], d["initial_state"],
-                              inp["scale"], inp["lower_bound"], o, fs, None, stream, raw_gates=a.raw_gates)
+                              inp["scale"], inp["lower_bound"], o, fs, None, stream, raw_gates=a.raw_gates,
+                              **norm_kw)
 
     for _ in range(max(3, a.warmup)):
         flush.zero_()
@@ -343,7 +353,7 @@ def bench_gpu(a, world, rank, local):
 
     # e2e through the C ABI with pinned host buffers (copies inside the timed region)
     host = {key: (None if inp[key] is None else inp[key].pin_memory()) for key in
-            ("q", "k", "v", "g", "beta", "cu_seqlens", "initial_state")}
+            ("q", "k", "v", "g", "beta", "cu_seqlens", "initial_state") + (("norm_gate",) if a.gated_norm else ())}
     o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
     fs_h = torch.empty(fs.shape, dtype=fs.dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in host.values() if t is not None)
@@ -372,11 +382,11 @@ def bench_gpu(a, world, rank, local):
     # roofline of the (single) kernel: algorithmic bytes per launch / mean launch time
     peaks = load_peaks()
     with_init = inp["initial_state"] is not None
-    alg_bytes = algorithmic_bytes(T, N, H, with_init)
+    alg_bytes = algorithmic_bytes(T, N, H, with_init) + (T * H * NORM_GATE_BYTES_PER_TOKEN_HEAD if a.gated_norm else 0)
     mean_launch_s = (sum(step_ms) / len(step_ms)) / 1e3
     achieved_gbs = alg_bytes / mean_launch_s / 1e9
     kernel = "kda_decode_kernel" if decode else "kda_persistent_kernel"
-    traffic = traffic_from_profile(a.workload, kernel)
+    traffic = None if a.gated_norm else traffic_from_profile(a.workload, kernel)
     flops = 0.0 if decode else algorithmic_flops(inp["seqlens"], H)
 
     out = None
@@ -391,7 +401,9 @@ def bench_gpu(a, world, rank, local):
             "vs_baseline": (value / world / PAGES_HEADLINE_TOKENS_PER_S) if a.workload == DEFAULT_WORKLOAD else None,
             "dtype": ("fp32 (bf16 q, k, v)" if decode else "bf16/fp16 (fp32 accumulate, fp32 state and o)"),
             "data": "synthetic", "config": dict(workload_config(a.workload, inp),
-                                                **({"gates": "raw, activated in the kernel"} if a.raw_gates else {})),
+                                                **({"gates": "raw, activated in the kernel"} if a.raw_gates else {}),
+                                                **({"output": "gated RMSNorm fused (bf16 gate, fp32 weight, eps 1e-5)"}
+                                                   if a.gated_norm else {})),
             "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": traffic,
                          "kernel": kernel, "algorithmic_bytes_per_launch": alg_bytes,
@@ -419,7 +431,11 @@ def main():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--raw-gates", action="store_true",
                    help="time kda_chunk_fwd_raw_gates (g and beta activated inside the kernel)")
+    p.add_argument("--gated-norm", action="store_true",
+                   help="time kda_chunk_fwd_gated_norm (the gated RMSNorm of o fused into the output store)")
     a = p.parse_args()
+    if a.raw_gates and a.gated_norm:
+        p.error("--raw-gates and --gated-norm are separate entry points")
     if a.warmup < 3:
         a.warmup = 3
     world, rank, local = dist_setup()

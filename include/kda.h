@@ -156,6 +156,36 @@ kda_status_t kda_chunk_fwd_raw_gates(const void *q, const void *k, const void *v
                                      float *final_state, int32_t *status_dev, void *workspace,
                                      size_t workspace_bytes, kda_stream_t stream);
 
+/*
+ * kda_chunk_fwd_gated_norm — kda_chunk_fwd with the gated RMSNorm of the
+ * output fused into the kernel's output store: the KDA output tail of the
+ * Kimi K3 PP16 prefill notes' flag table (the strided o-norm entry, which fuses
+ * FusedRMSNormGated with the copy its reshape forced). The page names the
+ * operation without writing it out; this library reads it as, per token t and
+ * head h over the 128 value channels c,
+ *     o[t][h][c] = x[t][h][c] / sqrt(mean_c(x[t][h][:]^2) + norm_eps)
+ *                  * norm_weight[c] * sigmoid(gate[t][h][c])
+ * where x is the attention output kda_chunk_fwd would write: an RMS
+ * normalisation over one head's value channels, a per-channel weight shared by
+ * the heads, and a sigmoid output gate.
+ *   gate         bf16 [total_tokens, num_heads, 128], 16-byte aligned
+ *   norm_weight  fp32 [128], 16-byte aligned
+ *   norm_eps     > 0 and finite (1e-5 is usual)
+ *   o            receives the normalised, gated output (fp32, as above); x is
+ *                not written anywhere
+ * final_state and every other argument, limit and error are as for
+ * kda_chunk_fwd. The norm runs in fp32 on the fp32 output rows; the sigmoid is
+ * evaluated as 1/2 + tanh(x/2)/2 on the packed fp16 hardware tanh (absolute
+ * error about 1e-3, below bf16's resolution at 1).
+ */
+kda_status_t kda_chunk_fwd_gated_norm(const void *q, const void *k, const void *v, const float *g,
+                                      const float *beta, const int32_t *cu_seqlens, int32_t num_seqs,
+                                      int64_t total_tokens, int32_t num_heads, int32_t head_dim_k,
+                                      int32_t head_dim_v, const float *initial_state, float scale,
+                                      float lower_bound, const void *gate, const float *norm_weight,
+                                      float norm_eps, float *o, float *final_state, int32_t *status_dev,
+                                      void *workspace, size_t workspace_bytes, kda_stream_t stream);
+
 /* Workspace bytes kda_chunk_fwd needs for these sizes on the current device
  * (0 when num_seqs or num_heads is 0, or no usable device is current). */
 size_t kda_chunk_fwd_workspace_size(int32_t num_seqs, int32_t num_heads);

@@ -29,7 +29,8 @@ KDA_DEBUG_WITHHOLD_READY = 1
 
 HEAD_DIM = 128
 EXPORTED = ("kda_chunk_fwd", "kda_chunk_fwd_workspace_size", "kda_chunk_fwd_static_scratch",
-            "kda_chunk_fwd_debug", "kda_chunk_fwd_raw_gates", "kda_decode_fwd", "kda_chunk_fwd_launches",
+            "kda_chunk_fwd_debug", "kda_chunk_fwd_raw_gates", "kda_chunk_fwd_gated_norm", "kda_decode_fwd",
+            "kda_chunk_fwd_launches",
             "kda_status_string", "kda_version")
 DECODE_MAX_TOKENS = 64
 
@@ -68,6 +69,9 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.kda_chunk_fwd_raw_gates.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i64, i32, i32, i32, vp, f32, f32,
                                                 vp, vp, vp, vp, ctypes.c_size_t, vp]
         lib.kda_chunk_fwd_raw_gates.restype = ctypes.c_int
+        lib.kda_chunk_fwd_gated_norm.argtypes = [vp, vp, vp, vp, vp, vp, i32, i64, i32, i32, i32, vp, f32, f32,
+                                                 vp, vp, f32, vp, vp, vp, vp, ctypes.c_size_t, vp]
+        lib.kda_chunk_fwd_gated_norm.restype = ctypes.c_int
         lib.kda_decode_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, f32, f32, vp, vp, vp, vp]
         lib.kda_decode_fwd.restype = ctypes.c_int
         lib.kda_chunk_fwd_workspace_size.argtypes = [i32, i32]
@@ -131,7 +135,8 @@ def _check(t, name, dtype, shape, device):
 
 def kda_chunk_fwd(q, k, v, g, beta, cu_seqlens, initial_state, scale: float, lower_bound: float,
                   o, final_state, status=None, stream=None, workspace=None, debug_flags: int = 0,
-                  raw_gates: bool = False, A_log=None, dt_bias=None) -> int:
+                  raw_gates: bool = False, A_log=None, dt_bias=None, norm_gate=None, norm_weight=None,
+                  norm_eps: float = 1e-5) -> int:
     """Call the C entry point ``kda_chunk_fwd`` with caller-allocated outputs.
 
     q, k, v: bf16 [T,H,128]; o: fp32 [T,H,128]; g: fp32 [T,H,128]; beta: fp32 [T,H];
@@ -144,7 +149,9 @@ def kda_chunk_fwd(q, k, v, g, beta, cu_seqlens, initial_state, scale: float, low
     (failure-detection testing; see include/kda.h). ``raw_gates=True`` calls
     ``kda_chunk_fwd_raw_gates``: ``g`` and ``beta`` are then the raw gate and
     beta projections, activated inside the kernel with the optional per-head
-    ``A_log`` (fp32 [H]) and ``dt_bias`` (fp32 [H,128]).
+    ``A_log`` (fp32 [H]) and ``dt_bias`` (fp32 [H,128]). Given ``norm_gate``
+    (bf16 [T,H,128]) and ``norm_weight`` (fp32 [128]), ``kda_chunk_fwd_gated_norm``
+    writes ``o`` as the gated RMSNorm of the output (``norm_eps`` inside the root).
     """
     T, H, D = q.shape
     N = cu_seqlens.shape[0] - 1
@@ -170,6 +177,14 @@ def kda_chunk_fwd(q, k, v, g, beta, cu_seqlens, initial_state, scale: float, low
         _check(A_log, "A_log", torch.float32, (H,), dev)
     if dt_bias is not None:
         _check(dt_bias, "dt_bias", torch.float32, (H, D), dev)
+    norm = norm_gate is not None or norm_weight is not None
+    if norm:
+        if norm_gate is None or norm_weight is None:
+            raise ValueError("norm_gate and norm_weight go together")
+        _check(norm_gate, "norm_gate", torch.bfloat16, tuple(v.shape), dev)
+        _check(norm_weight, "norm_weight", torch.float32, (v.shape[2],), dev)
+        if raw_gates or debug_flags:
+            raise ValueError("the gated norm combines with neither raw_gates nor debug_flags")
     if stream is None:
         stream = torch.cuda.current_stream(dev)
     if workspace is None:
@@ -180,7 +195,10 @@ def kda_chunk_fwd(q, k, v, g, beta, cu_seqlens, initial_state, scale: float, low
             _ptr(initial_state), float(scale), float(lower_bound), _ptr(o), _ptr(final_state),
             _ptr(status), _ptr(workspace), workspace.numel(), ctypes.c_void_p(stream.cuda_stream))
     lib = load_library()
-    if raw_gates:
+    if norm:
+        rc = lib.kda_chunk_fwd_gated_norm(*args[:14], _ptr(norm_gate), _ptr(norm_weight), float(norm_eps), *args[14:])
+        what = "kda_chunk_fwd_gated_norm"
+    elif raw_gates:
         if debug_flags:
             raise ValueError("debug_flags and raw_gates cannot be combined")
         rc = lib.kda_chunk_fwd_raw_gates(*args[:5], _ptr(A_log), _ptr(dt_bias), *args[5:])
@@ -195,13 +213,15 @@ def kda_chunk_fwd(q, k, v, g, beta, cu_seqlens, initial_state, scale: float, low
 
 def chunk_fwd(q, k, v, g, beta, cu_seqlens, initial_state=None, scale: Optional[float] = None,
               lower_bound: float = -5.0, output_final_state: bool = True, check: bool = False,
-              stream=None, raw_gates: bool = False, A_log=None, dt_bias=None):
+              stream=None, raw_gates: bool = False, A_log=None, dt_bias=None, norm_gate=None,
+              norm_weight=None, norm_eps: float = 1e-5):
     """Allocate ``o`` (and ``final_state``) and run ``kda_chunk_fwd``.
 
     Returns ``(o, final_state)``; ``final_state`` is None when not requested.
     With ``check=True`` the device status word is read back (a synchronising
     copy) and a device-detected error raises ``KdaError``. ``raw_gates``,
-    ``A_log`` and ``dt_bias`` are passed to ``kda_chunk_fwd``.
+    ``A_log``, ``dt_bias`` and the gated-norm arguments are passed to
+    ``kda_chunk_fwd``.
     """
     T, H, D = q.shape
     N = cu_seqlens.shape[0] - 1
@@ -212,7 +232,8 @@ def chunk_fwd(q, k, v, g, beta, cu_seqlens, initial_state=None, scale: Optional[
           if output_final_state else None)
     status = torch.zeros(1, dtype=torch.int32, device=q.device) if check else None
     kda_chunk_fwd(q, k, v, g, beta, cu_seqlens, initial_state, scale, lower_bound, o, fs, status, stream,
-                  raw_gates=raw_gates, A_log=A_log, dt_bias=dt_bias)
+                  raw_gates=raw_gates, A_log=A_log, dt_bias=dt_bias, norm_gate=norm_gate,
+                  norm_weight=norm_weight, norm_eps=norm_eps)
     if check:
         code = int(status.item())
         if code != KDA_OK:

@@ -21,12 +21,27 @@ bool lower_bound_ok(float lb) { return lb >= -10.9f && lb <= 0.0f; }
 }  // namespace
 
 namespace {
+// The options the entry points add to the plain forward.
+struct Extras {
+    uint32_t debug = 0;                 // KDA_DEBUG_* flags
+    bool raw = false;                   // g and beta are raw projections (kda_chunk_fwd_raw_gates)
+    const float *A_log = nullptr, *dt_bias = nullptr;
+    const void *norm_gate = nullptr;    // gated RMSNorm of o (kda_chunk_fwd_gated_norm)
+    const float *norm_weight = nullptr;
+    float norm_eps = 0.f;
+};
+
 kda_status_t fwd_impl(const void *q, const void *k, const void *v, const float *g, const float *beta,
                       const int32_t *cu_seqlens, int32_t num_seqs, int64_t total_tokens, int32_t num_heads,
                       int32_t head_dim_k, int32_t head_dim_v, const float *initial_state, float scale,
                       float lower_bound, float *o, float *final_state, int32_t *status_dev, void *workspace,
-                      size_t workspace_bytes, kda_stream_t stream, uint32_t debug_flags, bool raw = false,
-                      const float *A_log = nullptr, const float *dt_bias = nullptr) {
+                      size_t workspace_bytes, kda_stream_t stream, const Extras &x = Extras()) {
+    const float *A_log = x.A_log, *dt_bias = x.dt_bias;
+    if (x.norm_gate || x.norm_weight) {
+        if (!x.norm_gate || !x.norm_weight || !aligned(x.norm_gate, 16) || !aligned(x.norm_weight, 16))
+            return KDA_ERR_INVALID_ARG;
+        if (!(x.norm_eps > 0.f && x.norm_eps < 3.0e38f)) return KDA_ERR_INVALID_ARG;
+    }
     if (head_dim_k != KDA_HEAD_DIM || head_dim_v != KDA_HEAD_DIM) return KDA_ERR_UNSUPPORTED;
     if (num_seqs < 0 || total_tokens < 0 || num_heads < 1) return KDA_ERR_INVALID_ARG;
     if (static_cast<int64_t>(num_seqs) * num_heads > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
@@ -71,11 +86,14 @@ kda_status_t fwd_impl(const void *q, const void *k, const void *v, const float *
     p.status = status_dev;
     p.ws = static_cast<unsigned char *>(workspace);
     p.C = 0;
-    p.debug = debug_flags;
+    p.debug = x.debug;
     p.spin = 0;
-    p.raw = raw ? 1 : 0;
+    p.raw = x.raw ? 1 : 0;
     p.A_log = A_log;
     p.dt_bias = dt_bias;
+    p.ngate = static_cast<const __nv_bfloat16 *>(x.norm_gate);
+    p.nweight = x.norm_weight;
+    p.neps = x.norm_eps;
     const cudaError_t e = kda::pers::launch(p, workspace_bytes, s);
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
@@ -92,7 +110,7 @@ kda_status_t kda_chunk_fwd(const void *q, const void *k, const void *v, const fl
                            kda_stream_t stream) {
     return fwd_impl(q, k, v, g, beta, cu_seqlens, num_seqs, total_tokens, num_heads, head_dim_k, head_dim_v,
                     initial_state, scale, lower_bound, o, final_state, status_dev, workspace, workspace_bytes,
-                    stream, 0u);
+                    stream);
 }
 
 kda_status_t kda_chunk_fwd_debug(const void *q, const void *k, const void *v, const float *g,
@@ -103,9 +121,11 @@ kda_status_t kda_chunk_fwd_debug(const void *q, const void *k, const void *v, co
                                  int32_t *status_dev, void *workspace, size_t workspace_bytes,
                                  kda_stream_t stream, uint32_t debug_flags) {
     if (debug_flags & ~static_cast<uint32_t>(KDA_DEBUG_WITHHOLD_READY)) return KDA_ERR_INVALID_ARG;
+    Extras x;
+    x.debug = debug_flags;
     return fwd_impl(q, k, v, g, beta, cu_seqlens, num_seqs, total_tokens, num_heads, head_dim_k, head_dim_v,
                     initial_state, scale, lower_bound, o, final_state, status_dev, workspace, workspace_bytes,
-                    stream, debug_flags);
+                    stream, x);
 }
 
 kda_status_t kda_chunk_fwd_raw_gates(const void *q, const void *k, const void *v, const float *g_raw,
@@ -115,9 +135,30 @@ kda_status_t kda_chunk_fwd_raw_gates(const void *q, const void *k, const void *v
                                      const float *initial_state, float scale, float lower_bound, float *o,
                                      float *final_state, int32_t *status_dev, void *workspace,
                                      size_t workspace_bytes, kda_stream_t stream) {
+    Extras x;
+    x.raw = true;
+    x.A_log = A_log;
+    x.dt_bias = dt_bias;
     return fwd_impl(q, k, v, g_raw, beta_raw, cu_seqlens, num_seqs, total_tokens, num_heads, head_dim_k,
                     head_dim_v, initial_state, scale, lower_bound, o, final_state, status_dev, workspace,
-                    workspace_bytes, stream, 0u, true, A_log, dt_bias);
+                    workspace_bytes, stream, x);
+}
+
+kda_status_t kda_chunk_fwd_gated_norm(const void *q, const void *k, const void *v, const float *g,
+                                      const float *beta, const int32_t *cu_seqlens, int32_t num_seqs,
+                                      int64_t total_tokens, int32_t num_heads, int32_t head_dim_k,
+                                      int32_t head_dim_v, const float *initial_state, float scale,
+                                      float lower_bound, const void *gate, const float *norm_weight,
+                                      float norm_eps, float *o, float *final_state, int32_t *status_dev,
+                                      void *workspace, size_t workspace_bytes, kda_stream_t stream) {
+    if (!gate || !norm_weight) return KDA_ERR_INVALID_ARG;
+    Extras x;
+    x.norm_gate = gate;
+    x.norm_weight = norm_weight;
+    x.norm_eps = norm_eps;
+    return fwd_impl(q, k, v, g, beta, cu_seqlens, num_seqs, total_tokens, num_heads, head_dim_k, head_dim_v,
+                    initial_state, scale, lower_bound, o, final_state, status_dev, workspace, workspace_bytes,
+                    stream, x);
 }
 
 size_t kda_chunk_fwd_workspace_size(int32_t num_seqs, int32_t num_heads) {

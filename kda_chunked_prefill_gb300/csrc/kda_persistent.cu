@@ -988,9 +988,26 @@ constexpr int OFF_TMEM = OFF_BAR + 32;          // TMEM base address written by 
 constexpr int OFF_MISC = OFF_BAR + 64;
 constexpr int SMEM = OFF_MISC + 64;
 constexpr uint32_t TMEM_COLS = 256;
-constexpr int OST = 132;                        // fp32 row stride of the o staging tile (64 x OST spans S16 + v_new)
+constexpr int OST = 132;  // fp32 row stride of the o staging tile (64 x OST spans S16 + v_new); columns
+                          // 128-131 hold the row's four slice sums of squares for the gated norm
 static_assert(64 * OST * 4 <= 32768 + 16384, "o staging fits in the state and v_new tiles");
 __device__ __forceinline__ bool f16_ok(float x) { return fabsf(x) < F16_SAFE; }
+
+// one 128-byte line of global memory towards L2 (no register result)
+__device__ __forceinline__ void prefetch_l2(const void *ptr) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
+}
+// logistic function of a bf16 pair, as an fp16 pair: 1/2 + tanh(x/2)/2 with the
+// packed fp16 hardware tanh (one special-function operation per pair; absolute
+// error about 1e-3)
+__device__ __forceinline__ uint32_t sigmoid_bf16x2_to_f16x2(uint32_t g2) {
+    const float2 g = unpack_bf16(g2);
+    const uint32_t hx = pack_f16(0.5f * g.x, 0.5f * g.y);
+    uint32_t t, r;
+    asm("tanh.approx.f16x2 %0, %1;" : "=r"(t) : "r"(hx));
+    asm("fma.rn.f16x2 %0, %1, %2, %2;" : "=r"(r) : "r"(t), "r"(0x38003800u));  // t * 1/2 + 1/2
+    return r;
+}
 
 // completion of this CTA's own MMAs: depends on no other CTA, so only a
 // (bounded) timeout ends it early, never the abort word
@@ -1116,6 +1133,8 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
                 alive = false;
                 break;
             }
+            if (p.ngate && tid < 2 * BT && (tid >> 1) < nv)  // this chunk's gate rows (two lines each) -> L2
+                prefetch_l2(p.ngate + (static_cast<size_t>(t0 + (tid >> 1)) * p.H + h) * DV + 64 * (tid & 1));
             for (int it = 0; !mbar_try_wait(&full[b], (j >> 1) & 1); ++it)
                 if (it > (1 << 20)) {
                     set_status(p.status, KDA_ERR_TIMEOUT);
@@ -1219,7 +1238,20 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
             }
 
             // (6) o (TMEM lanes 0-63) -> staging in the (now free) state/v_new tiles ->
-            // global, one full 512-byte row per warp store
+            // global, one full 512-byte row per warp store. With the fused gated
+            // RMSNorm, warp w stores rows w, w+16, w+32, w+48: their gate values
+            // (this lane's four channels) are loaded before the wait, so that
+            // the loads land while MMA2/MMA3 run and o is staged.
+            static_assert(NCOMP / 32 * 4 == BT, "four output rows per warp");
+            uint2 gv[4];
+            if (p.ngate) {
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    const int rr = warp + 16 * q4;
+                    gv[q4] = rr < nv ? __ldg(reinterpret_cast<const uint2 *>(p.ngate + (static_cast<size_t>(t0 + rr) * p.H + h) * DV) + lane)
+                                     : make_uint2(0u, 0u);
+                }
+            }
             wait_all(R, bar_mma23, j & 1, p.status);
             tc_fence_after();
             KDA_TRACE_EV(p, 16, j);
@@ -1237,12 +1269,41 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
                     reinterpret_cast<float4 *>(dst + 16)[e] = make_float4(__uint_as_float(r1[4 * e]), __uint_as_float(r1[4 * e + 1]),
                                                                           __uint_as_float(r1[4 * e + 2]), __uint_as_float(r1[4 * e + 3]));
                 }
+                if (p.ngate) {  // this slice's sum of squares of the row, into the row's pad column 128 + slice
+                    float ss = 0.f;
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const float x0 = __uint_as_float(r0[e]), x1 = __uint_as_float(r1[e]);
+                        ss = fmaf(x0, x0, ss);
+                        ss = fmaf(x1, x1, ss);
+                    }
+                    stg[row * OST + DV + slice] = ss;
+                }
             }
             tc_fence_before();
             sync_compute();
-            for (int rr = warp; rr < nv; rr += NCOMP / 32)
-                reinterpret_cast<float4 *>(p.o + (static_cast<size_t>(t0 + rr) * p.H + h) * DV)[lane] =
-                    *reinterpret_cast<const float4 *>(stg + rr * OST + 4 * lane);
+            if (p.ngate) {
+                // y = x / sqrt(mean(x^2) + eps) * weight * sigmoid(gate) over the row's 128 channels
+                const float4 w4 = __ldg(reinterpret_cast<const float4 *>(p.nweight) + lane);
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    const int rr = warp + 16 * q4;
+                    if (rr < nv) {  // uniform in the warp
+                        const float4 x = *reinterpret_cast<const float4 *>(stg + rr * OST + 4 * lane);
+                        const float4 ps = *reinterpret_cast<const float4 *>(stg + rr * OST + DV);  // the four slices' sums
+                        const float rs = rsqrtf(((ps.x + ps.y) + (ps.z + ps.w)) * (1.f / DV) + p.neps);
+                        const float2 sa = unpack_f16(sigmoid_bf16x2_to_f16x2(gv[q4].x));
+                        const float2 sb = unpack_f16(sigmoid_bf16x2_to_f16x2(gv[q4].y));
+                        reinterpret_cast<float4 *>(p.o + (static_cast<size_t>(t0 + rr) * p.H + h) * DV)[lane] =
+                            make_float4(x.x * rs * w4.x * sa.x, x.y * rs * w4.y * sa.y, x.z * rs * w4.z * sb.x,
+                                        x.w * rs * w4.w * sb.y);
+                    }
+                }
+            } else {
+                for (int rr = warp; rr < nv; rr += NCOMP / 32)
+                    reinterpret_cast<float4 *>(p.o + (static_cast<size_t>(t0 + rr) * p.H + h) * DV)[lane] =
+                        *reinterpret_cast<const float4 *>(stg + rr * OST + 4 * lane);
+            }
             KDA_TRACE_EV(p, 12, j);
             if (tid == 0 && !issued_next && j + 1 < total) {
                 if (wait_flag_geq(R, &R.ready[k * RING + (j + 1) % RING], j + 2, p.status)) {

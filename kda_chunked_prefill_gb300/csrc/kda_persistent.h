@@ -30,6 +30,9 @@ struct Params {
     const float *A_log;  // [H] or NULL (raw mode)
     const float *dt_bias;  // [H][128] or NULL (raw mode)
     long long spin;      // polls before a wait gives up
+    const __nv_bfloat16 *ngate;  // [T][H][128] gate of the fused gated RMSNorm of o, or NULL (plain o)
+    const float *nweight;        // [128] its per-channel weight
+    float neps;                  // its epsilon
 };
 
 // workspace: [64-byte header][ready C*RING][freed C*RING] padded to 1024, then the slots

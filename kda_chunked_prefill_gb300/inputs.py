@@ -120,6 +120,16 @@ def make_inputs(seqlens, num_heads: int, seed: int, sigma_g: float = 1.0,
     }
 
 
+def make_norm_inputs(total_tokens: int, num_heads: int, seed: int, head_dim: int = HEAD_DIM) -> dict:
+    """The extra inputs of the fused gated RMSNorm of o: the output-gate
+    projection gate ~ N(0, 1.5^2) as bf16 [T,H,D], a per-channel weight
+    1 + N(0, 0.2^2) as fp32 [D], and eps = 1e-5. CPU torch tensors."""
+    rng = np.random.default_rng(seed)
+    gate = rng.standard_normal((total_tokens, num_heads, head_dim), dtype=np.float32) * np.float32(1.5)
+    weight = np.float32(1.0) + rng.standard_normal(head_dim, dtype=np.float32) * np.float32(0.2)
+    return {"gate": torch.from_numpy(gate).to(torch.bfloat16), "weight": torch.from_numpy(weight), "eps": 1e-5}
+
+
 def make_workload(wl: Workload) -> dict:
     rng = np.random.default_rng(wl.seed)
     if wl.seqlens is None:

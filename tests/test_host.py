@@ -132,6 +132,35 @@ def test_raw_gate_entry_validates_like_the_plain_call(lib, over, code):
     assert _call_raw(lib, **over) == code
 
 
+def _call_norm(lib, **over):
+    fake = ctypes.c_void_p(0x10000)
+    args = dict(q=fake, k=fake, v=fake, g=fake, beta=fake, cu=fake, N=2, T=100, H=4, dk=128, dv=128, s0=None,
+                scale=0.088, lb=-5.0, gate=fake, w=fake, eps=1e-5, o=fake, sT=None, status=None, ws=fake,
+                wsb=1 << 20, stream=None)
+    args.update(over)
+    return lib.kda_chunk_fwd_gated_norm(args["q"], args["k"], args["v"], args["g"], args["beta"], args["cu"],
+                                        args["N"], args["T"], args["H"], args["dk"], args["dv"], args["s0"],
+                                        args["scale"], args["lb"], args["gate"], args["w"], args["eps"], args["o"],
+                                        args["sT"], args["status"], args["ws"], args["wsb"], args["stream"])
+
+
+@pytest.mark.parametrize("over,code", [
+    ({"gate": None}, kda.KDA_ERR_INVALID_ARG),
+    ({"w": None}, kda.KDA_ERR_INVALID_ARG),
+    ({"gate": ctypes.c_void_p(0x10008)}, kda.KDA_ERR_INVALID_ARG),  # gate not 16-byte aligned
+    ({"w": ctypes.c_void_p(0x10004)}, kda.KDA_ERR_INVALID_ARG),     # weight not 16-byte aligned
+    ({"eps": 0.0}, kda.KDA_ERR_INVALID_ARG),
+    ({"eps": -1e-5}, kda.KDA_ERR_INVALID_ARG),
+    ({"eps": float("nan")}, kda.KDA_ERR_INVALID_ARG),
+    ({"eps": float("inf")}, kda.KDA_ERR_INVALID_ARG),
+    ({"dk": 64}, kda.KDA_ERR_UNSUPPORTED),
+    ({"g": None}, kda.KDA_ERR_INVALID_ARG),
+    ({"N": 0, "T": 0, "q": None, "k": None, "v": None, "g": None, "beta": None, "o": None}, kda.KDA_OK),
+])
+def test_gated_norm_entry_validates_its_arguments(lib, over, code):
+    assert _call_norm(lib, **over) == code
+
+
 def _call_decode(lib, **over):
     fake = ctypes.c_void_p(0x10000)
     args = dict(q=fake, k=fake, v=fake, g=fake, beta=fake, N=4, Tn=1, H=4, dk=128, dv=128, s0=None,
