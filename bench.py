@@ -316,8 +316,19 @@ def bench_gpu(a, world, rank, local):
     stream = torch.cuda.current_stream(dev)
     decode = wl.kind == "decode"
 
+    split_ws = None
+    split_L = 0
+    if a.split:  # the split-sequence scan, with its planned segment length
+        split_L = kda.split_plan(inp["cu_seqlens"], H)
+        split_ws = torch.empty(max(1, kda.split_workspace_size(inp["cu_seqlens"], H, 0)), dtype=torch.uint8,
+                               device=dev)
+
     def step():
-        if decode:
+        if a.split:
+            kda.kda_chunk_fwd_split(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], inp["cu_seqlens"],
+                                    d["initial_state"], inp["scale"], inp["lower_bound"], o, fs, None, stream,
+                                    segment_chunks=0, workspace=split_ws)
+        elif decode:
             kda.kda_decode_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], N, d["initial_state"], inp["scale"],
                                inp["lower_bound"], o, fs, None, stream)
         else:
@@ -386,7 +397,9 @@ def bench_gpu(a, world, rank, local):
     mean_launch_s = (sum(step_ms) / len(step_ms)) / 1e3
     achieved_gbs = alg_bytes / mean_launch_s / 1e9
     kernel = "kda_decode_kernel" if decode else "kda_persistent_kernel"
-    traffic = None if a.gated_norm else traffic_from_profile(a.workload, kernel)
+    traffic = None if (a.gated_norm or a.split) else traffic_from_profile(a.workload, kernel)
+    if a.split and split_L > 0:
+        kernel = "kda_persistent_kernel (two launches) + split combine"
     flops = 0.0 if decode else algorithmic_flops(inp["seqlens"], H)
 
     out = None
@@ -403,7 +416,8 @@ def bench_gpu(a, world, rank, local):
             "data": "synthetic", "config": dict(workload_config(a.workload, inp),
                                                 **({"gates": "raw, activated in the kernel"} if a.raw_gates else {}),
                                                 **({"output": "gated RMSNorm fused (bf16 gate, fp32 weight, eps 1e-5)"}
-                                                   if a.gated_norm else {})),
+                                                   if a.gated_norm else {}),
+                                                **({"split_segment_chunks": split_L} if a.split else {})),
             "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": traffic,
                          "kernel": kernel, "algorithmic_bytes_per_launch": alg_bytes,
@@ -414,7 +428,7 @@ def bench_gpu(a, world, rank, local):
                         "p90": sorted(step_ms)[(9 * len(step_ms)) // 10]},
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "steps": e2e_steps},
-            "gpu_launches": a.steps * (1 if decode else kda.chunk_fwd_launches(N, T, H)),
+            "gpu_launches": a.steps * (1 if decode else (5 if split_L > 0 else kda.chunk_fwd_launches(N, T, H))),
             "clocks": clocks,
             "cpu_baseline": cpu,
         }
@@ -431,11 +445,13 @@ def main():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--raw-gates", action="store_true",
                    help="time kda_chunk_fwd_raw_gates (g and beta activated inside the kernel)")
+    p.add_argument("--split", action="store_true",
+                   help="time kda_chunk_fwd_split (the split-sequence scan, planned segment length)")
     p.add_argument("--gated-norm", action="store_true",
                    help="time kda_chunk_fwd_gated_norm (the gated RMSNorm of o fused into the output store)")
     a = p.parse_args()
-    if a.raw_gates and a.gated_norm:
-        p.error("--raw-gates and --gated-norm are separate entry points")
+    if sum(map(bool, (a.raw_gates, a.gated_norm, a.split))) > 1:
+        p.error("--raw-gates, --gated-norm and --split are separate entry points")
     if a.warmup < 3:
         a.warmup = 3
     world, rank, local = dist_setup()

@@ -186,6 +186,64 @@ kda_status_t kda_chunk_fwd_gated_norm(const void *q, const void *k, const void *
                                       float norm_eps, float *o, float *final_state, int32_t *status_dev,
                                       void *workspace, size_t workspace_bytes, kda_stream_t stream);
 
+/*
+ * kda_chunk_fwd_split — kda_chunk_fwd for calls with few, long (sequence, head)
+ * chains, where the plain call runs each chain's chunks one after another on a
+ * few SMs (for example one long sequence with a few heads per GPU). Long
+ * sequences are cut at chunk boundaries into segments of `segment_chunks`
+ * chunks. The chunk recurrence of "在 TPU 上加速 Kimi K3 KDA" §6.2 is affine in
+ * the state, so a segment maps its entry state to its exit state as
+ * S_out = Phi S_in + N, and by linearity N is the exit state from a zero entry
+ * state and Phi + N the exit state from the identity. The call runs
+ *   1. one chunked launch over the segments except each sequence's last
+ *      (segment 0 from the sequence's entry state, the others from I and from
+ *      0), keeping only their exit states;
+ *   2. a combine kernel: S_1 = exit of segment 0, S_{s+1} = Phi_s S_s + N_s in
+ *      fp32;
+ *   3. one chunked launch over all segments as sequences of their own, from
+ *      their entry states S_s, writing o;
+ *   4. a copy of each sequence's last exit state into final_state.
+ *   cu_seqlens_host  host copy of cu_seqlens (int32 [num_seqs + 1]); the plan
+ *                    and the segment tables are built from it (validated: 0,
+ *                    nondecreasing, total_tokens). cu_seqlens (device) is read
+ *                    only when nothing is split.
+ *   segment_chunks   segment length in 64-token chunks; 0 lets the library
+ *                    choose (kda_chunk_fwd_split_plan); a sequence of more
+ *                    chunks is cut into segments of that length (at most 64;
+ *                    the last takes the rest). With no sequence cut, this is
+ *                    exactly kda_chunk_fwd.
+ *   workspace        at least kda_chunk_fwd_split_workspace_size(cu_seqlens_host,
+ *                    num_seqs, num_heads, segment_chunks) bytes, 256-byte
+ *                    aligned: the ring, the segment tables and four state arrays
+ *                    (about 4 x 64 KiB per segment and head).
+ * Other arguments, outputs and errors as kda_chunk_fwd (num_heads at most
+ * 65535). o and final_state agree with kda_chunk_fwd within the parity
+ * tolerance, not bitwise (the entry states come through the fp32 combine).
+ * Launches: 1 without a cut; otherwise 4, plus 1 when final_state is given,
+ * plus one host-to-device copy of the tables (from pageable memory, staged
+ * before the call returns).
+ */
+kda_status_t kda_chunk_fwd_split(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                                 const int32_t *cu_seqlens, const int32_t *cu_seqlens_host, int32_t num_seqs,
+                                 int64_t total_tokens, int32_t num_heads, int32_t head_dim_k, int32_t head_dim_v,
+                                 const float *initial_state, float scale, float lower_bound, int32_t segment_chunks,
+                                 float *o, float *final_state, int32_t *status_dev, void *workspace,
+                                 size_t workspace_bytes, kda_stream_t stream);
+
+/* The segment length (chunks) kda_chunk_fwd_split picks for these lengths on a
+ * GPU with num_sms SMs (0: the current device), from the measured paces of the
+ * chunked kernel (a busy consumer SM finishes a chunk every 3.5 us, a producer
+ * SM every 7.0 us, a launch costs about 15 us); 0 when no segment length is
+ * estimated to beat the plain call by 20 %, or the arguments are invalid. */
+int32_t kda_chunk_fwd_split_plan(const int32_t *cu_seqlens_host, int32_t num_seqs, int32_t num_heads,
+                                 int32_t num_sms);
+
+/* Workspace bytes of kda_chunk_fwd_split for these lengths and segment length
+ * (0: the planned one) on the current device; 0 on invalid arguments or when no
+ * usable device is current. */
+size_t kda_chunk_fwd_split_workspace_size(const int32_t *cu_seqlens_host, int32_t num_seqs, int32_t num_heads,
+                                          int32_t segment_chunks);
+
 /* Workspace bytes kda_chunk_fwd needs for these sizes on the current device
  * (0 when num_seqs or num_heads is 0, or no usable device is current). */
 size_t kda_chunk_fwd_workspace_size(int32_t num_seqs, int32_t num_heads);

@@ -29,7 +29,8 @@ KDA_DEBUG_WITHHOLD_READY = 1
 
 HEAD_DIM = 128
 EXPORTED = ("kda_chunk_fwd", "kda_chunk_fwd_workspace_size", "kda_chunk_fwd_static_scratch",
-            "kda_chunk_fwd_debug", "kda_chunk_fwd_raw_gates", "kda_chunk_fwd_gated_norm", "kda_decode_fwd",
+            "kda_chunk_fwd_debug", "kda_chunk_fwd_raw_gates", "kda_chunk_fwd_gated_norm", "kda_chunk_fwd_split",
+            "kda_chunk_fwd_split_plan", "kda_chunk_fwd_split_workspace_size", "kda_decode_fwd",
             "kda_chunk_fwd_launches",
             "kda_status_string", "kda_version")
 DECODE_MAX_TOKENS = 64
@@ -72,6 +73,13 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.kda_chunk_fwd_gated_norm.argtypes = [vp, vp, vp, vp, vp, vp, i32, i64, i32, i32, i32, vp, f32, f32,
                                                  vp, vp, f32, vp, vp, vp, vp, ctypes.c_size_t, vp]
         lib.kda_chunk_fwd_gated_norm.restype = ctypes.c_int
+        lib.kda_chunk_fwd_split.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i64, i32, i32, i32, vp, f32, f32, i32,
+                                            vp, vp, vp, vp, ctypes.c_size_t, vp]
+        lib.kda_chunk_fwd_split.restype = ctypes.c_int
+        lib.kda_chunk_fwd_split_plan.argtypes = [vp, i32, i32, i32]
+        lib.kda_chunk_fwd_split_plan.restype = ctypes.c_int32
+        lib.kda_chunk_fwd_split_workspace_size.argtypes = [vp, i32, i32, i32]
+        lib.kda_chunk_fwd_split_workspace_size.restype = ctypes.c_size_t
         lib.kda_decode_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, f32, f32, vp, vp, vp, vp]
         lib.kda_decode_fwd.restype = ctypes.c_int
         lib.kda_chunk_fwd_workspace_size.argtypes = [i32, i32]
@@ -238,6 +246,93 @@ def chunk_fwd(q, k, v, g, beta, cu_seqlens, initial_state=None, scale: Optional[
         code = int(status.item())
         if code != KDA_OK:
             raise KdaError(code, "kda_chunk_fwd (device)")
+    return o, fs
+
+
+def _host_cu(cu_seqlens_host):
+    cu = torch.as_tensor(cu_seqlens_host, dtype=torch.int32).cpu().contiguous()
+    return cu, ctypes.c_void_p(cu.data_ptr())
+
+
+def split_plan(cu_seqlens_host, num_heads: int, num_sms: int = 0) -> int:
+    """Segment length (in 64-token chunks) ``kda_chunk_fwd_split`` would pick
+    for these sequence lengths (0: no split). ``num_sms`` 0 = the current device."""
+    cu, ptr = _host_cu(cu_seqlens_host)
+    return int(load_library().kda_chunk_fwd_split_plan(ptr, cu.numel() - 1, int(num_heads), int(num_sms)))
+
+
+def split_workspace_size(cu_seqlens_host, num_heads: int, segment_chunks: int = 0) -> int:
+    cu, ptr = _host_cu(cu_seqlens_host)
+    return int(load_library().kda_chunk_fwd_split_workspace_size(ptr, cu.numel() - 1, int(num_heads),
+                                                                  int(segment_chunks)))
+
+
+def kda_chunk_fwd_split(q, k, v, g, beta, cu_seqlens, cu_seqlens_host, initial_state, scale: float,
+                        lower_bound: float, o, final_state, status=None, stream=None, segment_chunks: int = 0,
+                        workspace=None) -> int:
+    """Call ``kda_chunk_fwd_split`` (the split-sequence scan; see include/kda.h).
+    Arguments as ``kda_chunk_fwd`` plus ``cu_seqlens_host`` (the same offsets on
+    the host: a CPU tensor, array or list) and ``segment_chunks`` (0: planned).
+    ``workspace`` defaults to a fresh uint8 tensor of the needed size."""
+    T, H, D = q.shape
+    dev = q.device
+    cu, cu_ptr = _host_cu(cu_seqlens_host)
+    N = cu.numel() - 1
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    _check(q, "q", torch.bfloat16, (T, H, D), dev)
+    _check(k, "k", torch.bfloat16, (T, H, D), dev)
+    _check(v, "v", torch.bfloat16, (T, H, v.shape[2]), dev)
+    _check(g, "g", torch.float32, (T, H, D), dev)
+    _check(beta, "beta", torch.float32, (T, H), dev)
+    _check(cu_seqlens, "cu_seqlens", torch.int32, (N + 1,), dev)
+    _check(o, "o", torch.float32, tuple(v.shape), dev)
+    for t, name in ((initial_state, "initial_state"), (final_state, "final_state")):
+        if t is not None:
+            _check(t, name, torch.float32, (N, H, D, v.shape[2]), dev)
+    if status is not None:
+        _check(status, "status", torch.int32, (1,), dev)
+    lib = load_library()
+    if workspace is None:
+        nbytes = lib.kda_chunk_fwd_split_workspace_size(cu_ptr, N, H, int(segment_chunks))
+        if nbytes == 0:
+            raise KdaError(KDA_ERR_INVALID_ARG, "kda_chunk_fwd_split_workspace_size")
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    if workspace.device != dev or workspace.dtype != torch.uint8 or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous uint8 tensor on the inputs' device")
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    rc = lib.kda_chunk_fwd_split(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), cu_ptr, N, T, H,
+                                 D, v.shape[2], _ptr(initial_state), float(scale), float(lower_bound),
+                                 int(segment_chunks), _ptr(o), _ptr(final_state), _ptr(status), _ptr(workspace),
+                                 workspace.numel(), ctypes.c_void_p(stream.cuda_stream))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_chunk_fwd_split")
+    return rc
+
+
+def chunk_fwd_split(q, k, v, g, beta, cu_seqlens, cu_seqlens_host=None, initial_state=None,
+                    scale: Optional[float] = None, lower_bound: float = -5.0, output_final_state: bool = True,
+                    check: bool = False, stream=None, segment_chunks: int = 0):
+    """Allocate ``o`` (and ``final_state``) and run ``kda_chunk_fwd_split``.
+    ``cu_seqlens_host`` defaults to a copy of ``cu_seqlens`` (a synchronising
+    device-to-host read)."""
+    T, H, D = q.shape
+    if cu_seqlens_host is None:
+        cu_seqlens_host = cu_seqlens.cpu()
+    N = cu_seqlens.shape[0] - 1
+    if scale is None:
+        scale = D ** -0.5
+    o = torch.empty((T, H, v.shape[2]), dtype=torch.float32, device=q.device)
+    fs = (torch.empty((N, H, D, v.shape[2]), dtype=torch.float32, device=q.device)
+          if output_final_state else None)
+    status = torch.zeros(1, dtype=torch.int32, device=q.device) if check else None
+    kda_chunk_fwd_split(q, k, v, g, beta, cu_seqlens, cu_seqlens_host, initial_state, scale, lower_bound, o, fs,
+                        status, stream, segment_chunks=segment_chunks)
+    if check:
+        code = int(status.item())
+        if code != KDA_OK:
+            raise KdaError(code, "kda_chunk_fwd_split (device)")
     return o, fs
 
 

@@ -77,6 +77,8 @@ kda_status_t fwd_impl(const void *q, const void *k, const void *v, const float *
     p.cu = cu_seqlens;
     p.N = num_seqs;
     p.T = total_tokens;
+    p.seq_bos = nullptr;
+    p.Ttok = total_tokens;
     p.H = num_heads;
     p.s0 = initial_state;
     p.scale = scale;

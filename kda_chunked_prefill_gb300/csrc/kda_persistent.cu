@@ -164,17 +164,20 @@ __device__ __forceinline__ void drain_mbar(uint64_t *bar, uint32_t parity) {
 }
 
 // chunks of chain ch (sequence ch / H), or -1 when its bounds are invalid;
-// `cu` is p.cu or a copy of it in shared memory
+// `cu` is p.cu or a copy of it in shared memory. The sequence's first token is
+// cu[n], or seq_bos[n] when that map is given.
 __device__ __forceinline__ int chain_info(const Params &p, const int32_t *cu, int ch, int64_t &bos, int64_t &len) {
     const int n = ch / p.H;
     const int64_t b = cu[n], e = cu[n + 1];
-    const bool bad = b < 0 || e < b || e > p.T || (n == 0 && b != 0) || (n == p.N - 1 && e != p.T);
+    const int64_t s = p.seq_bos ? static_cast<int64_t>(p.seq_bos[n]) : b;
+    const bool bad = b < 0 || e < b || e > p.T || (n == 0 && b != 0) || (n == p.N - 1 && e != p.T) || s < 0 ||
+                     s + (e - b) > p.Ttok;
     if (bad) {
         bos = 0;
         len = 0;
         return -1;
     }
-    bos = b;
+    bos = s;
     len = e - b;
     return static_cast<int>((len + BT - 1) / BT);
 }
@@ -1282,7 +1285,9 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
             }
             tc_fence_before();
             sync_compute();
-            if (p.ngate) {
+            if (!p.o) {
+                // states only: no output rows
+            } else if (p.ngate) {
                 // y = x / sqrt(mean(x^2) + eps) * weight * sigmoid(gate) over the row's 128 channels
                 const float4 w4 = __ldg(reinterpret_cast<const float4 *>(p.nweight) + lane);
 #pragma unroll

@@ -20,7 +20,7 @@ struct Params {
     int32_t H;
     const float *s0;
     float scale, lb;
-    float *o, *sT;
+    float *o, *sT;       // o may be NULL (nothing written but the final states)
     int32_t *status;
     unsigned char *ws;
     int32_t C;           // consumer CTAs (set by launch)
@@ -30,6 +30,9 @@ struct Params {
     const float *A_log;  // [H] or NULL (raw mode)
     const float *dt_bias;  // [H][128] or NULL (raw mode)
     long long spin;      // polls before a wait gives up
+    const int32_t *seq_bos;  // [N] first token of each sequence, or NULL (cu[n]); with it, cu gives
+                             // only the lengths and sequences may cover the same tokens
+    int64_t Ttok;            // tokens in q, k, v, g, beta (bounds seq_bos ranges)
     const __nv_bfloat16 *ngate;  // [T][H][128] gate of the fused gated RMSNorm of o, or NULL (plain o)
     const float *nweight;        // [128] its per-channel weight
     float neps;                  // its epsilon

@@ -54,7 +54,8 @@ def _lognormal_lengths(rng, n: int) -> List[int]:
 
 
 def workloads() -> dict:
-    """The named workloads (tiny, headline, cached-prefix, batch sweep, wide; decode steps)."""
+    """The named workloads (tiny, headline, cached-prefix, batch sweep, wide, long;
+    decode steps)."""
     w = {
         "tiny_T256_H2": Workload("tiny_T256_H2", (256,), 1, 2, seed=0),
         "headline_4x2048_H16": Workload("headline_4x2048_H16", (2048,) * 4, 4, 16, seed=1),
@@ -67,6 +68,9 @@ def workloads() -> dict:
     }
     for b in (1, 2, 4, 8, 16, 32, 64):
         w[f"sweep_B{b}_H16"] = Workload(f"sweep_B{b}_H16", None, b, 16, seed=b)
+    # one long sequence with the few heads one GPU holds under head-parallel
+    # sharding: few, long chains (the split-sequence scan's case)
+    w["long_1x65536_H4"] = Workload("long_1x65536_H4", (65536,), 1, 4, seed=5, state_std=0.02)
     # decode steps: one new token per sequence on a carried state
     w["decode_B256_H16"] = Workload("decode_B256_H16", (1,) * 256, 256, 16, seed=9, state_std=0.02, kind="decode")
     w["decode_B64x4_H16"] = Workload("decode_B64x4_H16", (4,) * 64, 64, 16, seed=10, state_std=0.02, kind="decode")

@@ -6,6 +6,8 @@ import os
 import re
 import subprocess
 
+import numpy as np
+
 import pytest
 
 import kda_chunked_prefill_gb300 as kda
@@ -159,6 +161,61 @@ def _call_norm(lib, **over):
 ])
 def test_gated_norm_entry_validates_its_arguments(lib, over, code):
     assert _call_norm(lib, **over) == code
+
+
+def _cu(lens):
+    return [0] + list(np.cumsum(lens).astype(int))
+
+
+def test_split_plan_leaves_the_producer_bound_workloads_alone():
+    """The configured prefill workloads are paced by the producers or balanced:
+    the planner splits none of them (on 152 SMs), but it splits the long
+    few-head workload and single long sequences with few heads."""
+    from kda_chunked_prefill_gb300 import inputs as kin
+    for name, w in kin.workloads().items():
+        if w.kind != "prefill" or name.startswith("long_"):
+            continue
+        assert kda.split_plan(_cu(kin.seqlens_for(w)), w.num_heads, 152) == 0, name
+    L = kda.split_plan(_cu([65536]), 4, 152)
+    assert L > 0 and 2 <= -(-1024 // L) <= 64
+    assert kda.split_plan(_cu([65536, 500, 70]), 4, 152) > 0
+    assert kda.split_plan(_cu([16384]), 16, 152) == 0
+
+
+def test_split_plan_rejects_bad_offsets():
+    assert kda.split_plan([0, 10, 5], 4, 152) == 0
+    assert kda.split_plan([1, 10], 4, 152) == 0
+    assert kda.split_workspace_size([0, 10, 5], 4, 2) == 0
+
+
+def _call_split(lib, cu_host, **over):
+    fake = ctypes.c_void_p(0x10000)
+    cu_arr = (ctypes.c_int32 * len(cu_host))(*cu_host)
+    args = dict(q=fake, k=fake, v=fake, g=fake, beta=fake, cu=fake, cuh=ctypes.cast(cu_arr, ctypes.c_void_p),
+                N=len(cu_host) - 1, T=cu_host[-1], H=4, dk=128, dv=128, s0=None, scale=0.088, lb=-5.0, L=2,
+                o=fake, sT=None, status=None, ws=fake, wsb=1 << 30, stream=None)
+    args.update(over)
+    return lib.kda_chunk_fwd_split(args["q"], args["k"], args["v"], args["g"], args["beta"], args["cu"], args["cuh"],
+                                   args["N"], args["T"], args["H"], args["dk"], args["dv"], args["s0"], args["scale"],
+                                   args["lb"], args["L"], args["o"], args["sT"], args["status"], args["ws"],
+                                   args["wsb"], args["stream"])
+
+
+@pytest.mark.parametrize("cu_host,over,code", [
+    ([0, 1000, 1200], {"dk": 64}, kda.KDA_ERR_UNSUPPORTED),
+    ([0, 1000, 1200], {"H": 70000}, kda.KDA_ERR_UNSUPPORTED),
+    ([0, 1000, 1200], {"L": -1}, kda.KDA_ERR_INVALID_ARG),
+    ([0, 1000, 900], {}, kda.KDA_ERR_INVALID_ARG),         # host offsets decrease
+    ([5, 1000, 1200], {}, kda.KDA_ERR_INVALID_ARG),        # do not start at 0
+    ([0, 1000, 1200], {"T": 1300}, kda.KDA_ERR_INVALID_ARG),  # do not end at total_tokens
+    ([0, 1000, 1200], {"cuh": None}, kda.KDA_ERR_INVALID_ARG),
+    ([0, 1000, 1200], {"q": None}, kda.KDA_ERR_INVALID_ARG),
+    ([0, 1000, 1200], {"ws": ctypes.c_void_p(0x10010)}, kda.KDA_ERR_INVALID_ARG),  # workspace not 256-aligned
+    ([0, 1000, 1200], {"o": ctypes.c_void_p(0x10008)}, kda.KDA_ERR_INVALID_ARG),
+    ([0, 1000, 1200], {"lb": -20.0}, kda.KDA_ERR_INVALID_ARG),
+])
+def test_split_entry_validates_its_arguments(lib, cu_host, over, code):
+    assert _call_split(lib, cu_host, **over) == code
 
 
 def _call_decode(lib, **over):
