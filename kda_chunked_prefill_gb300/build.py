@@ -10,6 +10,7 @@ import concurrent.futures as cf
 import glob
 import hashlib
 import os
+import re
 import shutil
 import subprocess
 import sys
@@ -47,13 +48,29 @@ def _stamp() -> str:
     return h.hexdigest()
 
 
+def _local_includes(path: str, seen: set) -> None:
+    """Add `path` and, transitively, the csrc headers it includes with quotes."""
+    if path in seen:
+        return
+    seen.add(path)
+    with open(path, encoding="utf-8") as fh:
+        for line in fh:
+            m = re.match(r'\s*#\s*include\s+"([^"]+)"', line)
+            if m:
+                dep = os.path.join(CSRC, m.group(1))
+                if os.path.exists(dep):
+                    _local_includes(dep, seen)
+
+
 def kernel_stamp(source: str) -> str:
-    """Hash of one kernel's translation unit: its .cu file, the shared device
-    headers it can include, and the compile flags. A change elsewhere (another
-    kernel, the host API, documentation) leaves it unchanged."""
+    """Hash of one kernel's translation unit: its .cu file, the csrc headers it
+    includes (transitively), and the compile flags. A change elsewhere (another
+    kernel, the host API and its documentation in include/, a header this file
+    does not include) leaves it unchanged."""
+    files: set = set()
+    _local_includes(os.path.join(CSRC, source), files)
     h = hashlib.sha256()
-    for f in [os.path.join(CSRC, source)] + sorted(glob.glob(os.path.join(CSRC, "*.cuh"))) + \
-            sorted(glob.glob(os.path.join(CSRC, "*.h"))):
+    for f in sorted(files):
         h.update(os.path.relpath(f, ROOT).encode())
         with open(f, "rb") as fh:
             h.update(fh.read())
