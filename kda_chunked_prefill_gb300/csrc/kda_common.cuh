@@ -40,31 +40,12 @@ __device__ __forceinline__ float2 unpack_f16(uint32_t u) {
     return __half22float2(p);
 }
 
-// x = hi + lo with hi = bf16(x) and lo = bf16(x - hi): about 16 significant bits
-// in two bf16 operands, with bf16's exponent range.
-__device__ __forceinline__ void split_bf16(float x0, float x1, uint32_t &hi, uint32_t &lo) {
-    const __nv_bfloat16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
-    const float r0 = x0 - __bfloat162float(h0), r1 = x1 - __bfloat162float(h1);
-    __nv_bfloat162 h;
-    h.x = h0;
-    h.y = h1;
-    hi = *reinterpret_cast<uint32_t *>(&h);
-    lo = pack_bf16(r0, r1);
-}
-
 // Largest magnitude kept below fp16's finite limit (65504) with margin.
 constexpr float F16_SAFE = 60000.f;
 
 __device__ __forceinline__ float2 unpack_bf16(uint32_t u) {
     __nv_bfloat162 p = *reinterpret_cast<__nv_bfloat162 *>(&u);
     return __bfloat1622float2(p);
-}
-
-// round to the nearest tf32 value (ties away from zero); low 13 bits cleared
-__device__ __forceinline__ uint32_t to_tf32(float x) {
-    uint32_t y;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(y) : "f"(x));
-    return y;
 }
 
 // 4-byte global -> shared copy; src_bytes = 0 writes zero.
@@ -106,7 +87,6 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// D += A(16x16, row) * B(16x8, col), fp16 inputs, fp32 accumulate.
 // d += a * b on tf32 operands (m16n8k8): a0 (row g, k q), a1 (row g+8, k q),
 // a2 (row g, k q+4), a3 (row g+8, k q+4); b0 (k q, col g), b1 (k q+4, col g);
 // g = lane / 4, q = lane % 4
@@ -117,6 +97,7 @@ __device__ __forceinline__ void mma1688_tf32(float (&d)[4], const uint32_t (&a)[
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
+// D += A(16x16, row) * B(16x8, col), fp16 inputs, fp32 accumulate.
 __device__ __forceinline__ void mma16816_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
     asm volatile(
         "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
@@ -125,23 +106,11 @@ __device__ __forceinline__ void mma16816_f16(float (&d)[4], const uint32_t (&a)[
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// Fragment addressing (lane = threadIdx.x % 32) for a 16x16 tile at (row0,col0)
-// of a row-major bf16 matrix with row stride `ld` elements.
-//  A operand, stored [m][k]:                 ldsm_x4  at  a_addr
-//  A operand, stored transposed [k][m]:      ldsm_x4_t at at_addr
-//  B operand (two n8 tiles), stored [n][k]:  ldsm_x4  at  bn_addr
-//  B operand (two n8 tiles), stored [k][n]:  ldsm_x4_t at bk_addr
-__device__ __forceinline__ int a_off(int lane, int row0, int col0, int ld) {
-    return (row0 + (lane & 15)) * ld + col0 + ((lane >> 4) << 3);
-}
-__device__ __forceinline__ int at_off(int lane, int m0, int k0, int ld) {
-    const int mi = lane >> 3, r = lane & 7;
-    return (k0 + ((mi >> 1) << 3) + r) * ld + m0 + ((mi & 1) << 3);
-}
-__device__ __forceinline__ int bn_off(int lane, int n0, int k0, int ld) {
-    const int mi = lane >> 3, r = lane & 7;
-    return (n0 + ((mi >> 1) << 3) + r) * ld + k0 + ((mi & 1) << 3);
-}
+// Fragment addressing (lane = threadIdx.x % 32) of the B operand (two n8
+// tiles) of a 16x16 tile at (k0, n0), stored [k][n] in a row-major 16-bit
+// matrix with row stride `ld` elements: the element offset ldsm_x4_t takes.
+// (The swizzled tiles of the prefill kernel have their own a_addr / at_addr /
+// bk_addr.)
 __device__ __forceinline__ int bk_off(int lane, int k0, int n0, int ld) {
     const int mi = lane >> 3, r = lane & 7;
     return (k0 + ((mi & 1) << 3) + r) * ld + n0 + ((mi >> 1) << 3);
@@ -182,10 +151,6 @@ __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
 }
 __device__ __forceinline__ void mbar_fence_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
-    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_u32(bar))
-                 : "memory");
 }
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
     asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(
@@ -239,19 +204,6 @@ __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wa
 __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
     return static_cast<uint64_t>((saddr >> 4) & 0x3FFF) | (static_cast<uint64_t>((lbo >> 4) & 0x3FFF) << 16) |
            (static_cast<uint64_t>((sbo >> 4) & 0x3FFF) << 32) | (1ull << 46) | (2ull << 61);
-}
-// Instruction descriptor, kind::tf32 (A, B tf32; D fp32), both K-major.
-__device__ __forceinline__ uint32_t umma_idesc_tf32(int M, int N) {
-    return (1u << 4) | (2u << 7) | (2u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
-           (static_cast<uint32_t>(M >> 4) << 24);
-}
-// D (+)= A * B with A read from tensor memory (lane = row, one 32-bit column per K element)
-__device__ __forceinline__ void umma_tf32_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
-                                             uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate));
 }
 // Instruction descriptor, kind::f16 with fp16 A/B and fp32 D.
 __device__ __forceinline__ uint32_t umma_idesc_f16(bool a_mn_major, bool b_mn_major, int M, int N) {
