@@ -76,6 +76,33 @@ def test_cached_prefix_workload_all_heads():
     check_case(kin.make_workload(kin.workloads()["cached_prefix_B16_H16"]))
 
 
+def test_cached_prefix_every_sequence_on_its_own():
+    """The parity bar applied to each sequence's o and final_state separately
+    (each against its own RMS), not only to the whole tensors; the worst
+    values are written as JSON to the file KDA_PARITY_REPORT names, if set."""
+    import json
+    import os
+    inp = kin.make_workload(kin.workloads()["cached_prefix_B16_H16"])
+    o, fs = pu.run_gpu(inp)
+    ref_o, ref_s = pu.run_oracle(inp)
+    o = o.float().cpu().numpy()
+    fs = fs.cpu().numpy()
+    cu = inp["cu_seqlens"].numpy()
+    worst = {"o_rel_l2": 0.0, "o_maxabs_over_rms": 0.0, "S_rel_l2": 0.0, "S_maxabs_over_rms": 0.0}
+    for n in range(len(cu) - 1):
+        a, b = int(cu[n]), int(cu[n + 1])
+        eo = pu.assert_parity(o[a:b], ref_o[a:b], f"o of sequence {n} ({b - a} tokens)")
+        es = pu.assert_parity(fs[n], ref_s[n], f"final_state of sequence {n}")
+        worst["o_rel_l2"] = max(worst["o_rel_l2"], eo["rel_l2"])
+        worst["o_maxabs_over_rms"] = max(worst["o_maxabs_over_rms"], eo["max_abs"] / eo["rms_ref"])
+        worst["S_rel_l2"] = max(worst["S_rel_l2"], es["rel_l2"])
+        worst["S_maxabs_over_rms"] = max(worst["S_maxabs_over_rms"], es["max_abs"] / es["rms_ref"])
+    report = os.environ.get("KDA_PARITY_REPORT")
+    if report:
+        with open(report, "w") as f:
+            json.dump({"workload": "cached_prefix_B16_H16", "worst_over_sequences": worst}, f, indent=1)
+
+
 @pytest.mark.parametrize("b", [1, 2, 4, 8, 16, 32, 64])
 def test_batch_sweep_workload(b):
     inp = kin.make_workload(kin.workloads()[f"sweep_B{b}_H16"])
