@@ -205,6 +205,34 @@ def test_split_and_carry_state_equals_full_run(cut):
     np.testing.assert_allclose(sb, sT, rtol=1e-13, atol=1e-14)
 
 
+def test_segment_exit_state_is_affine_in_its_entry_state():
+    """The reading behind the split-sequence scan: a segment maps its entry
+    state S to Phi S + N, with N its exit state from a zero entry state and
+    Phi + N its exit state from the identity; chaining three segments this way
+    reproduces the full run's final state, and each segment's o from its
+    composed entry state reproduces the full run's o. Computed on the oracle
+    with K = V = 12 (the identity needs K = V)."""
+    rng = np.random.default_rng(21)
+    K = 12
+    q, k, v, g, beta, cu, s0 = rand_case(rng, [150], 2, K, K)
+    o, sT = oracle.kda_recurrence(q, k, v, g, beta, cu, s0, 0.3)
+    eye = np.broadcast_to(np.eye(K), (1, 2, K, K)).copy()
+    cuts = [0, 64, 128, 150]
+    S = s0
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        sl = slice(a, b)
+        args = (q[sl], k[sl], v[sl], g[sl], beta[sl], [0, b - a])
+        _, n0 = oracle.kda_recurrence(*args, None, 0.3)
+        _, fi = oracle.kda_recurrence(*args, eye, 0.3)
+        phi = fi - n0
+        o_seg, s_seg = oracle.kda_recurrence(*args, S, 0.3)
+        np.testing.assert_allclose(o_seg, o[sl], rtol=1e-12, atol=1e-13)
+        S_next = np.einsum("nhij,nhjc->nhic", phi, S) + n0
+        np.testing.assert_allclose(S_next, s_seg, rtol=1e-12, atol=1e-13)
+        S = S_next
+    np.testing.assert_allclose(S, sT, rtol=1e-12, atol=1e-13)
+
+
 def test_linear_in_value_and_state_jointly():
     rng = np.random.default_rng(8)
     q, k, v, g, beta, cu, s0 = rand_case(rng, [45, 19], 2, 8, 8)
