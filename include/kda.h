@@ -244,6 +244,47 @@ int32_t kda_chunk_fwd_split_plan(const int32_t *cu_seqlens_host, int32_t num_seq
 size_t kda_chunk_fwd_split_workspace_size(const int32_t *cu_seqlens_host, int32_t num_seqs, int32_t num_heads,
                                           int32_t segment_chunks);
 
+/*
+ * kda_chunk_fwd_host — kda_chunk_fwd on inputs and outputs in HOST memory, with
+ * the transfers overlapped with the computation (a deployment convenience of
+ * this library; the pages have no counterpart). The sequences are cut into
+ * `groups` groups of whole sequences with about equal token counts (0: 4;
+ * at most 16 and num_seqs). Group i's q, k, v, g, beta and initial states are
+ * copied to the device on h2d_stream; `stream` waits for them and runs the
+ * chunked kernel on that group alone; d2h_stream waits for that launch and
+ * copies the group's o and final states back. Copies of neighbouring groups
+ * thus run while a group computes. `stream` finally waits for the last copy
+ * back: when it is synchronised, o and final_state hold the results.
+ *   q .. beta, initial_state, o, final_state  host memory, layouts as in
+ *                   kda_chunk_fwd; page-locked memory lets the copies overlap
+ *                   (with pageable memory they still complete, but serialise).
+ *                   final_state may alias initial_state.
+ *   cu_seqlens_host host int32 [num_seqs + 1] (validated: 0, nondecreasing,
+ *                   total_tokens).
+ *   device_buffer   device memory of at least kda_chunk_fwd_host_buffer_size(...)
+ *                   bytes, 256-byte aligned: device copies of every input and
+ *                   output, the rebased offsets and the kernel's workspace; not
+ *                   to be shared by calls that overlap on the GPU.
+ *   h2d_stream, d2h_stream  streams for the copies in and out (NULL: `stream`,
+ *                   which serialises the copies with the computation).
+ *   status_dev      optional device int32, as for kda_chunk_fwd.
+ * Creates and releases 2 x groups + 2 CUDA events per call (no memory).
+ * Returns KDA_OK once everything is queued, or a host-side error code.
+ */
+kda_status_t kda_chunk_fwd_host(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                                const int32_t *cu_seqlens_host, int32_t num_seqs, int64_t total_tokens,
+                                int32_t num_heads, int32_t head_dim_k, int32_t head_dim_v,
+                                const float *initial_state, float scale, float lower_bound, float *o,
+                                float *final_state, int32_t *status_dev, void *device_buffer,
+                                size_t device_buffer_bytes, int32_t groups, kda_stream_t stream,
+                                kda_stream_t h2d_stream, kda_stream_t d2h_stream);
+
+/* Device buffer bytes of kda_chunk_fwd_host for these lengths (with or without
+ * initial and final states, and `groups` as in the call) on the current device;
+ * 0 on invalid arguments or when no usable device is current. */
+size_t kda_chunk_fwd_host_buffer_size(const int32_t *cu_seqlens_host, int32_t num_seqs, int32_t num_heads,
+                                      int32_t with_initial_state, int32_t with_final_state, int32_t groups);
+
 /* Workspace bytes kda_chunk_fwd needs for these sizes on the current device
  * (0 when num_seqs or num_heads is 0, or no usable device is current). */
 size_t kda_chunk_fwd_workspace_size(int32_t num_seqs, int32_t num_heads);

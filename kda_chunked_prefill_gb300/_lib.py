@@ -30,7 +30,8 @@ KDA_DEBUG_WITHHOLD_READY = 1
 HEAD_DIM = 128
 EXPORTED = ("kda_chunk_fwd", "kda_chunk_fwd_workspace_size", "kda_chunk_fwd_static_scratch",
             "kda_chunk_fwd_debug", "kda_chunk_fwd_raw_gates", "kda_chunk_fwd_gated_norm", "kda_chunk_fwd_split",
-            "kda_chunk_fwd_split_plan", "kda_chunk_fwd_split_workspace_size", "kda_decode_fwd",
+            "kda_chunk_fwd_split_plan", "kda_chunk_fwd_split_workspace_size", "kda_chunk_fwd_host",
+            "kda_chunk_fwd_host_buffer_size", "kda_decode_fwd",
             "kda_chunk_fwd_launches",
             "kda_status_string", "kda_version")
 DECODE_MAX_TOKENS = 64
@@ -80,6 +81,11 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.kda_chunk_fwd_split_plan.restype = ctypes.c_int32
         lib.kda_chunk_fwd_split_workspace_size.argtypes = [vp, i32, i32, i32]
         lib.kda_chunk_fwd_split_workspace_size.restype = ctypes.c_size_t
+        lib.kda_chunk_fwd_host.argtypes = [vp, vp, vp, vp, vp, vp, i32, i64, i32, i32, i32, vp, f32, f32, vp, vp, vp,
+                                           vp, ctypes.c_size_t, i32, vp, vp, vp]
+        lib.kda_chunk_fwd_host.restype = ctypes.c_int
+        lib.kda_chunk_fwd_host_buffer_size.argtypes = [vp, i32, i32, i32, i32, i32]
+        lib.kda_chunk_fwd_host_buffer_size.restype = ctypes.c_size_t
         lib.kda_decode_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, f32, f32, vp, vp, vp, vp]
         lib.kda_decode_fwd.restype = ctypes.c_int
         lib.kda_chunk_fwd_workspace_size.argtypes = [i32, i32]
@@ -334,6 +340,51 @@ def chunk_fwd_split(q, k, v, g, beta, cu_seqlens, cu_seqlens_host=None, initial_
         if code != KDA_OK:
             raise KdaError(code, "kda_chunk_fwd_split (device)")
     return o, fs
+
+
+def host_buffer_size(cu_seqlens_host, num_heads: int, with_initial_state: bool, with_final_state: bool = True,
+                     groups: int = 0) -> int:
+    cu, ptr = _host_cu(cu_seqlens_host)
+    return int(load_library().kda_chunk_fwd_host_buffer_size(ptr, cu.numel() - 1, int(num_heads),
+                                                              int(bool(with_initial_state)),
+                                                              int(bool(with_final_state)), int(groups)))
+
+
+def kda_chunk_fwd_host(q, k, v, g, beta, cu_seqlens_host, initial_state, scale: float, lower_bound: float, o,
+                       final_state, device_buffer, status=None, groups: int = 0, stream=None, h2d_stream=None,
+                       d2h_stream=None) -> int:
+    """Call ``kda_chunk_fwd_host``: q .. beta, initial_state, o and final_state
+    are CPU tensors (page-locked for overlap; layouts as ``kda_chunk_fwd``),
+    ``device_buffer`` a CUDA uint8 tensor of ``host_buffer_size(...)`` bytes.
+    The results are in ``o`` / ``final_state`` once ``stream`` is synchronised."""
+    T, H, D = q.shape
+    cu, cu_ptr = _host_cu(cu_seqlens_host)
+    N = cu.numel() - 1
+    cpu = torch.device("cpu")
+    _check(q, "q", torch.bfloat16, (T, H, D), cpu)
+    _check(k, "k", torch.bfloat16, (T, H, D), cpu)
+    _check(v, "v", torch.bfloat16, (T, H, v.shape[2]), cpu)
+    _check(g, "g", torch.float32, (T, H, D), cpu)
+    _check(beta, "beta", torch.float32, (T, H), cpu)
+    _check(o, "o", torch.float32, tuple(v.shape), cpu)
+    for t, name in ((initial_state, "initial_state"), (final_state, "final_state")):
+        if t is not None:
+            _check(t, name, torch.float32, (N, H, D, v.shape[2]), cpu)
+    dev = device_buffer.device
+    if dev.type != "cuda" or device_buffer.dtype != torch.uint8 or not device_buffer.is_contiguous():
+        raise ValueError("device_buffer must be a contiguous CUDA uint8 tensor")
+    if status is not None:
+        _check(status, "status", torch.int32, (1,), dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    sp = lambda s_: None if s_ is None else ctypes.c_void_p(s_.cuda_stream)
+    rc = load_library().kda_chunk_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), cu_ptr, N, T, H, D,
+                                           v.shape[2], _ptr(initial_state), float(scale), float(lower_bound), _ptr(o),
+                                           _ptr(final_state), _ptr(status), _ptr(device_buffer), device_buffer.numel(),
+                                           int(groups), sp(stream), sp(h2d_stream), sp(d2h_stream))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_chunk_fwd_host")
+    return rc
 
 
 def kda_decode_fwd(q, k, v, g, beta, num_seqs: int, initial_state, scale: float, lower_bound: float,

@@ -218,6 +218,36 @@ def test_split_entry_validates_its_arguments(lib, cu_host, over, code):
     assert _call_split(lib, cu_host, **over) == code
 
 
+def _call_host(lib, cu_host, **over):
+    fake = ctypes.c_void_p(0x10000)
+    cu_arr = (ctypes.c_int32 * len(cu_host))(*cu_host)
+    args = dict(q=fake, k=fake, v=fake, g=fake, beta=fake, cuh=ctypes.cast(cu_arr, ctypes.c_void_p),
+                N=len(cu_host) - 1, T=cu_host[-1], H=4, dk=128, dv=128, s0=None, scale=0.088, lb=-5.0, o=fake,
+                sT=None, status=None, buf=ctypes.c_void_p(0x100000), bufb=1 << 30, G=0, stream=None, h2d=None,
+                d2h=None)
+    args.update(over)
+    return lib.kda_chunk_fwd_host(args["q"], args["k"], args["v"], args["g"], args["beta"], args["cuh"], args["N"],
+                                  args["T"], args["H"], args["dk"], args["dv"], args["s0"], args["scale"], args["lb"],
+                                  args["o"], args["sT"], args["status"], args["buf"], args["bufb"], args["G"],
+                                  args["stream"], args["h2d"], args["d2h"])
+
+
+@pytest.mark.parametrize("cu_host,over,code", [
+    ([0, 100, 300], {"dk": 64}, kda.KDA_ERR_UNSUPPORTED),
+    ([0, 100, 300], {"G": -1}, kda.KDA_ERR_INVALID_ARG),
+    ([0, 100, 90], {}, kda.KDA_ERR_INVALID_ARG),             # host offsets decrease
+    ([0, 100, 300], {"T": 301}, kda.KDA_ERR_INVALID_ARG),    # do not end at total_tokens
+    ([0, 100, 300], {"cuh": None}, kda.KDA_ERR_INVALID_ARG),
+    ([0, 100, 300], {"q": None}, kda.KDA_ERR_INVALID_ARG),
+    ([0, 100, 300], {"buf": None}, kda.KDA_ERR_INVALID_ARG),
+    ([0, 100, 300], {"buf": ctypes.c_void_p(0x100010)}, kda.KDA_ERR_INVALID_ARG),  # not 256-byte aligned
+    ([0, 100, 300], {"lb": 0.5}, kda.KDA_ERR_INVALID_ARG),
+    ([0, 100, 300], {"scale": float("nan")}, kda.KDA_ERR_INVALID_ARG),
+])
+def test_host_buffer_entry_validates_its_arguments(lib, cu_host, over, code):
+    assert _call_host(lib, cu_host, **over) == code
+
+
 def _call_decode(lib, **over):
     fake = ctypes.c_void_p(0x10000)
     args = dict(q=fake, k=fake, v=fake, g=fake, beta=fake, N=4, Tn=1, H=4, dk=128, dv=128, s0=None,
