@@ -5,18 +5,14 @@
 
 #include "kda.h"
 
+#include "kda_checks.h"
 #include "kda_persistent.h"
 
 namespace {
 
 constexpr int32_t kVersion = 100;  // 0.1.0
-
-constexpr int64_t kKdaMaxTokens = 0x7fffffffLL - 64;
-bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
-
-// The strip products form factors up to 2^(8*|lower_bound|/ln 2); keep that
-// below 2^126 so they stay finite in bf16 and fp32.
-bool lower_bound_ok(float lb) { return lb >= -10.9f && lb <= 0.0f; }
+using kda::checks::aligned;
+using kda::checks::lower_bound_ok;
 
 }  // namespace
 
@@ -47,7 +43,7 @@ kda_status_t fwd_impl(const void *q, const void *k, const void *v, const float *
     if (static_cast<int64_t>(num_seqs) * num_heads > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
     if (total_tokens > (int64_t{1} << 40) / (static_cast<int64_t>(num_heads) * KDA_HEAD_DIM))
         return KDA_ERR_INVALID_ARG;
-    if (total_tokens > kKdaMaxTokens) return KDA_ERR_UNSUPPORTED;  // task token offsets are 32-bit
+    if (total_tokens > kda::checks::kMaxTokens) return KDA_ERR_UNSUPPORTED;  // task token offsets are 32-bit
     if (!(scale == scale) || !lower_bound_ok(lower_bound)) return KDA_ERR_INVALID_ARG;
     if (num_seqs == 0) return total_tokens == 0 ? KDA_OK : KDA_ERR_INVALID_ARG;
     if (!cu_seqlens || !aligned(cu_seqlens, 4)) return KDA_ERR_INVALID_ARG;

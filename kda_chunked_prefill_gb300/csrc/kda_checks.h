@@ -1,0 +1,29 @@
+// Host-side argument checks shared by the C entry points (include/kda.h).
+#pragma once
+#include <stdint.h>
+
+namespace kda {
+namespace checks {
+
+// Most tokens a call may hold: the per-chunk tasks address tokens with 32-bit
+// offsets (plus a chunk of headroom).
+constexpr int64_t kMaxTokens = 0x7fffffffLL - 64;
+
+inline bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// The strip products form factors up to 2^(8 |lower_bound| / ln 2); keep that
+// below 2^126 so they stay finite in bf16 and fp32.
+inline bool lower_bound_ok(float lb) { return lb >= -10.9f && lb <= 0.0f; }
+
+inline bool scale_ok(float s) { return s == s; }
+
+// A host copy of cu_seqlens: starts at 0, never decreases, ends at T.
+inline bool host_seqlens_ok(const int32_t *cu, int32_t N, int64_t T) {
+    if (!cu || N < 0 || cu[0] != 0 || cu[N] != T) return false;
+    for (int32_t n = 0; n < N; ++n)
+        if (cu[n + 1] < cu[n]) return false;
+    return true;
+}
+
+}  // namespace checks
+}  // namespace kda

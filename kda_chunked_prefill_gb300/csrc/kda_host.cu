@@ -16,6 +16,7 @@
 
 #include "kda.h"
 
+#include "kda_checks.h"
 #include "kda_persistent.h"
 
 namespace kda {
@@ -23,7 +24,8 @@ namespace host {
 
 constexpr int DK = 128, DV = 128, MAX_GROUPS = 16;
 constexpr size_t STATE = static_cast<size_t>(DK) * DV;
-constexpr int64_t kMaxTokens = 0x7fffffffLL - 64;
+using checks::kMaxTokens;
+using checks::host_seqlens_ok;
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
@@ -67,13 +69,6 @@ Layout layout_for(const int32_t *cu, int N, int H, bool with_init, bool with_fin
     return l;
 }
 
-bool host_seqlens_ok(const int32_t *cu, int32_t N, int64_t T) {
-    if (!cu || cu[0] != 0 || cu[N] != T) return false;
-    for (int n = 0; n < N; ++n)
-        if (cu[n + 1] < cu[n]) return false;
-    return true;
-}
-
 int groups_for(int N, int32_t groups) {
     const int G = groups > 0 ? groups : 4;
     return std::max(1, std::min({G, N, MAX_GROUPS}));
@@ -106,10 +101,10 @@ kda_status_t kda_chunk_fwd_host(const void *q, const void *k, const void *v, con
     if (num_seqs < 1 || num_heads < 1 || total_tokens < 0 || groups < 0) return KDA_ERR_INVALID_ARG;
     if (total_tokens > kMaxTokens) return KDA_ERR_UNSUPPORTED;
     if (!host_seqlens_ok(cu_seqlens_host, num_seqs, total_tokens)) return KDA_ERR_INVALID_ARG;
-    if (!(scale == scale) || !(lower_bound >= -10.9f && lower_bound <= 0.0f)) return KDA_ERR_INVALID_ARG;
+    if (!kda::checks::scale_ok(scale) || !kda::checks::lower_bound_ok(lower_bound)) return KDA_ERR_INVALID_ARG;
     if (total_tokens > 0 && (!q || !k || !v || !g || !beta || !o)) return KDA_ERR_INVALID_ARG;
-    if (!device_buffer || (reinterpret_cast<uintptr_t>(device_buffer) % 256) != 0) return KDA_ERR_INVALID_ARG;
-    if (status_dev && (reinterpret_cast<uintptr_t>(status_dev) % 4) != 0) return KDA_ERR_INVALID_ARG;
+    if (!device_buffer || !kda::checks::aligned(device_buffer, 256)) return KDA_ERR_INVALID_ARG;
+    if (status_dev && !kda::checks::aligned(status_dev, 4)) return KDA_ERR_INVALID_ARG;
     const int N = num_seqs, H = num_heads;
     const std::vector<int> first = group_bounds(cu_seqlens_host, N, groups_for(N, groups));
     const int G = static_cast<int>(first.size()) - 1;

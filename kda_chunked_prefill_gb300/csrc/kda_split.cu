@@ -23,6 +23,7 @@
 
 #include "kda.h"
 
+#include "kda_checks.h"
 #include "kda_persistent.h"
 
 namespace kda {
@@ -31,7 +32,7 @@ namespace split {
 constexpr int BT = 64, DK = 128, DV = 128;
 constexpr size_t STATE = static_cast<size_t>(DK) * DV;  // floats per (sequence, head) state
 constexpr int MAX_SEGMENTS = 64;                        // per sequence
-constexpr int64_t kMaxTokens = 0x7fffffffLL - 64;
+using checks::kMaxTokens;
 
 // Measured paces of the chunked kernel on GB300 (the same model picks its
 // consumer count): a busy consumer finishes a chunk every 3.5 us, a producer
@@ -225,14 +226,8 @@ __global__ void __launch_bounds__(256) gather_final(const int32_t *segp, const i
     for (int e = threadIdx.x; e < static_cast<int>(STATE / 4); e += blockDim.x) dst[e] = src[e];
 }
 
-bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
-
-bool host_seqlens_ok(const int32_t *cu, int32_t N, int64_t T) {
-    if (!cu || cu[0] != 0 || cu[N] != T) return false;
-    for (int n = 0; n < N; ++n)
-        if (cu[n + 1] < cu[n]) return false;
-    return true;
-}
+using checks::aligned;
+using checks::host_seqlens_ok;
 
 int current_sms() {
     int dev = 0, sms = 0;
@@ -285,7 +280,7 @@ kda_status_t kda_chunk_fwd_split(const void *q, const void *k, const void *v, co
                              workspace_bytes, stream);
     // the checks kda_chunk_fwd makes, for the pointers the passes use
     if (total_tokens > kMaxTokens || z.t1 > kMaxTokens) return KDA_ERR_UNSUPPORTED;
-    if (!(scale == scale) || !(lower_bound >= -10.9f && lower_bound <= 0.0f)) return KDA_ERR_INVALID_ARG;
+    if (!kda::checks::scale_ok(scale) || !kda::checks::lower_bound_ok(lower_bound)) return KDA_ERR_INVALID_ARG;
     if (!q || !k || !v || !g || !beta || !o || !workspace) return KDA_ERR_INVALID_ARG;
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(g, 16) || !aligned(o, 16) ||
         !aligned(beta, 4) || !aligned(workspace, 256) || (initial_state && !aligned(initial_state, 16)) ||
