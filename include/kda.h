@@ -289,8 +289,11 @@ size_t kda_chunk_fwd_host_buffer_size(const int32_t *cu_seqlens_host, int32_t nu
  * (0 when num_seqs or num_heads is 0, or no usable device is current). */
 size_t kda_chunk_fwd_workspace_size(int32_t num_seqs, int32_t num_heads);
 
-/* Size of the fixed device scratch array behind kda_chunk_fwd_static_scratch. */
+/* Size of the fixed device scratch array behind kda_chunk_fwd_static_scratch
+ * (a build may define a different size). */
+#ifndef KDA_STATIC_SCRATCH_BYTES
 #define KDA_STATIC_SCRATCH_BYTES (24u << 20)
+#endif
 
 /*
  * kda_chunk_fwd_static_scratch — kda_chunk_fwd for callers that cannot allocate
@@ -306,8 +309,9 @@ size_t kda_chunk_fwd_workspace_size(int32_t num_seqs, int32_t num_heads);
  * the library, which every GPU that loads the library holds until the process
  * exits. No call allocates or frees memory.
  *
- * The first call made on a device looks up the array's device address with
- * cudaGetSymbolAddress while that device is current; make that first call
+ * Each call looks up the array's device address with cudaGetSymbolAddress on
+ * the current device (so a reset device context is no problem); the first
+ * call on a device also loads the library's device code there, so make it
  * before any stream capture. Every call on a device shares the one array and
  * it keeps the previous call's contents (the part that must start at zero is
  * cleared on the stream by each call), so calls whose GPU work may overlap

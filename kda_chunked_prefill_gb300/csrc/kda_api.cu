@@ -12,9 +12,37 @@ namespace {
 
 constexpr int32_t kVersion = 100;  // 0.1.0
 using kda::checks::aligned;
-using kda::checks::lower_bound_ok;
 
 }  // namespace
+
+namespace kda {
+namespace checks {
+kda_status_t fwd_args(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                      const int32_t *cu_seqlens, int32_t num_seqs, int64_t total_tokens, int32_t num_heads,
+                      int32_t head_dim_k, int32_t head_dim_v, const float *initial_state, float scale,
+                      float lower_bound, const float *o, const float *final_state, const int32_t *status_dev) {
+    if (head_dim_k != KDA_HEAD_DIM || head_dim_v != KDA_HEAD_DIM) return KDA_ERR_UNSUPPORTED;
+    if (num_seqs < 0 || total_tokens < 0 || num_heads < 1) return KDA_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(num_seqs) * num_heads > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
+    if (total_tokens > (int64_t{1} << 40) / (static_cast<int64_t>(num_heads) * KDA_HEAD_DIM))
+        return KDA_ERR_INVALID_ARG;
+    if (total_tokens > kMaxTokens) return KDA_ERR_UNSUPPORTED;  // task token offsets are 32-bit
+    if (!scale_ok(scale) || !lower_bound_ok(lower_bound)) return KDA_ERR_INVALID_ARG;
+    if (num_seqs == 0) return total_tokens == 0 ? KDA_OK : KDA_ERR_INVALID_ARG;
+    if (!cu_seqlens || !aligned(cu_seqlens, 4)) return KDA_ERR_INVALID_ARG;
+    if (total_tokens > 0) {
+        if (!q || !k || !v || !g || !beta || !o) return KDA_ERR_INVALID_ARG;
+        if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(g, 16) || !aligned(o, 16) ||
+            !aligned(beta, 4))
+            return KDA_ERR_INVALID_ARG;
+    }
+    if ((initial_state && !aligned(initial_state, 16)) || (final_state && !aligned(final_state, 16)) ||
+        (status_dev && !aligned(status_dev, 4)))
+        return KDA_ERR_INVALID_ARG;
+    return KDA_OK;
+}
+}  // namespace checks
+}  // namespace kda
 
 namespace {
 // The options the entry points add to the plain forward.
@@ -38,24 +66,12 @@ kda_status_t fwd_impl(const void *q, const void *k, const void *v, const float *
             return KDA_ERR_INVALID_ARG;
         if (!(x.norm_eps > 0.f && x.norm_eps < 3.0e38f)) return KDA_ERR_INVALID_ARG;
     }
-    if (head_dim_k != KDA_HEAD_DIM || head_dim_v != KDA_HEAD_DIM) return KDA_ERR_UNSUPPORTED;
-    if (num_seqs < 0 || total_tokens < 0 || num_heads < 1) return KDA_ERR_INVALID_ARG;
-    if (static_cast<int64_t>(num_seqs) * num_heads > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
-    if (total_tokens > (int64_t{1} << 40) / (static_cast<int64_t>(num_heads) * KDA_HEAD_DIM))
-        return KDA_ERR_INVALID_ARG;
-    if (total_tokens > kda::checks::kMaxTokens) return KDA_ERR_UNSUPPORTED;  // task token offsets are 32-bit
-    if (!(scale == scale) || !lower_bound_ok(lower_bound)) return KDA_ERR_INVALID_ARG;
-    if (num_seqs == 0) return total_tokens == 0 ? KDA_OK : KDA_ERR_INVALID_ARG;
-    if (!cu_seqlens || !aligned(cu_seqlens, 4)) return KDA_ERR_INVALID_ARG;
-    if (total_tokens > 0) {
-        if (!q || !k || !v || !g || !beta || !o) return KDA_ERR_INVALID_ARG;
-        if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(g, 16) ||
-            !aligned(o, 16) || !aligned(beta, 4))
-            return KDA_ERR_INVALID_ARG;
-    }
-    if ((initial_state && !aligned(initial_state, 16)) || (final_state && !aligned(final_state, 16)) ||
-        (status_dev && !aligned(status_dev, 4)) || (A_log && !aligned(A_log, 4)) || (dt_bias && !aligned(dt_bias, 16)))
-        return KDA_ERR_INVALID_ARG;
+    const kda_status_t args = kda::checks::fwd_args(q, k, v, g, beta, cu_seqlens, num_seqs, total_tokens, num_heads,
+                                                    head_dim_k, head_dim_v, initial_state, scale, lower_bound, o,
+                                                    final_state, status_dev);
+    if (args != KDA_OK) return args;
+    if (num_seqs == 0) return KDA_OK;
+    if ((A_log && !aligned(A_log, 4)) || (dt_bias && !aligned(dt_bias, 16))) return KDA_ERR_INVALID_ARG;
     if (!workspace || !aligned(workspace, 16)) return KDA_ERR_INVALID_ARG;
     const size_t need = kda::pers::workspace_bytes(static_cast<int64_t>(num_seqs) * num_heads);
     if (need == 0) return KDA_ERR_CUDA;

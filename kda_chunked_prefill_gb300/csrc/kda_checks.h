@@ -2,6 +2,8 @@
 #pragma once
 #include <stdint.h>
 
+#include "kda.h"
+
 namespace kda {
 namespace checks {
 
@@ -24,6 +26,15 @@ inline bool host_seqlens_ok(const int32_t *cu, int32_t N, int64_t T) {
         if (cu[n + 1] < cu[n]) return false;
     return true;
 }
+
+// The host-side checks of kda_chunk_fwd's arguments (everything but the
+// workspace pair), in the order the entry point applies them: KDA_OK when the
+// call may proceed (num_seqs == 0 with total_tokens == 0 included: a call with
+// nothing to do), otherwise the status the entry point returns.
+kda_status_t fwd_args(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                      const int32_t *cu_seqlens, int32_t num_seqs, int64_t total_tokens, int32_t num_heads,
+                      int32_t head_dim_k, int32_t head_dim_v, const float *initial_state, float scale,
+                      float lower_bound, const float *o, const float *final_state, const int32_t *status_dev);
 
 }  // namespace checks
 }  // namespace kda

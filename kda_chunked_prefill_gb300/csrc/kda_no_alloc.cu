@@ -12,47 +12,34 @@
 // The array is a file-scope __device__ variable: every GPU that loads this
 // library holds KDA_STATIC_SCRATCH_BYTES of it until the process exits. In host
 // code the array's name only stands in for the symbol; its device address is
-// obtained once per device with cudaGetSymbolAddress while that device is
-// current (on the first call made on that device) and passed to the kernel.
+// looked up with cudaGetSymbolAddress on every call, with the call's device
+// current, and passed to the kernel. (A cached address would go stale when the
+// device's primary context is reset and the module reloaded at a new address;
+// the lookup is a cheap query once the module is loaded.)
 #include <cuda_runtime.h>
-
-#include <mutex>
 
 #include "kda.h"
 
-static __device__ __align__(256) unsigned char kda_static_scratch[KDA_STATIC_SCRATCH_BYTES];
+#include "kda_checks.h"
 
-namespace {
-constexpr int kMaxDevices = 64;
-std::mutex g_setup_mutex;
-void *g_scratch_addr[kMaxDevices] = {};
-}  // namespace
+static __device__ __align__(256) unsigned char kda_static_scratch[KDA_STATIC_SCRATCH_BYTES];
 
 extern "C" kda_status_t kda_chunk_fwd_static_scratch(
     const void *q, const void *k, const void *v, const float *g, const float *beta,
     const int32_t *cu_seqlens, int32_t num_seqs, int64_t total_tokens, int32_t num_heads,
     int32_t head_dim_k, int32_t head_dim_v, const float *initial_state, float scale,
     float lower_bound, float *o, float *final_state, int32_t *status_dev, kda_stream_t stream) {
-    if (num_seqs < 1 || num_heads < 1)  // nothing to schedule: the ordinary path handles it
-        return kda_chunk_fwd(q, k, v, g, beta, cu_seqlens, num_seqs, total_tokens, num_heads, head_dim_k,
-                             head_dim_v, initial_state, scale, lower_bound, o, final_state, status_dev,
-                             nullptr, 0, stream);
+    // the same argument checks, in the same order, as kda_chunk_fwd
+    const kda_status_t args = kda::checks::fwd_args(q, k, v, g, beta, cu_seqlens, num_seqs, total_tokens, num_heads,
+                                                    head_dim_k, head_dim_v, initial_state, scale, lower_bound, o,
+                                                    final_state, status_dev);
+    if (args != KDA_OK) return args;
+    if (num_seqs == 0) return KDA_OK;  // nothing to schedule
     const size_t need = kda_chunk_fwd_workspace_size(num_seqs, num_heads);
     if (need == 0) return KDA_ERR_CUDA;  // no usable device is current
     if (need > static_cast<size_t>(KDA_STATIC_SCRATCH_BYTES)) return KDA_ERR_SCRATCH_TOO_SMALL;
-
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KDA_ERR_CUDA;
     void *scratch = nullptr;
-    {
-        std::lock_guard<std::mutex> lock(g_setup_mutex);
-        if (!g_scratch_addr[dev]) {
-            void *addr = nullptr;
-            if (cudaGetSymbolAddress(&addr, kda_static_scratch) != cudaSuccess || !addr) return KDA_ERR_CUDA;
-            g_scratch_addr[dev] = addr;
-        }
-        scratch = g_scratch_addr[dev];
-    }
+    if (cudaGetSymbolAddress(&scratch, kda_static_scratch) != cudaSuccess || !scratch) return KDA_ERR_CUDA;
     // kda_chunk_fwd clears the scratch's flag area on the stream before its launch,
     // so nothing left in the array by an earlier call is read as valid.
     return kda_chunk_fwd(q, k, v, g, beta, cu_seqlens, num_seqs, total_tokens, num_heads, head_dim_k,
