@@ -416,7 +416,7 @@ constexpr uint32_t TM_RV = 0, TM_RK = 64, TM_XU = 128, TM_XW = 192, TM_COLS = 25
 // ten tiles (three on partitions 0 and 1, two on 2 and 3); the diagonal
 // inverses run on warps 10, 11, 14, 15 (partitions 2 and 3) and the zero tiles
 // of Aqk on warps 12 and 13 (partitions 0 and 1).
-constexpr int SYNC_TID = 13 * 32;             // lane 0 of warp 13: draws tasks
+constexpr int SYNC_TID = 9 * 32;              // lane 0 of warp 9: draws tasks
 constexpr int REL_TID = 12 * 32;              // lane 0 of warp 12: publishes slots, waits for free slots
 // byte offset of the 16-byte chunk holding channels [c4, c4+4) of row r of the g tile
 __device__ __forceinline__ int g_chunk(int r, int c4) {
@@ -473,37 +473,54 @@ __device__ __forceinline__ Task fetch_task(const Params &p, const unsigned char 
     return t;
 }
 
+// 32 bytes of row r of a 128-byte-swizzled tile with `rows` rows per atom
+// column: the 16 16-bit elements at columns c16 .. c16 + 15 (c16 a multiple of
+// 16). Their two 16-byte chunks are adjacent in memory (in swapped order when
+// the row's swizzle is odd), so one 32-byte store writes a whole sector.
+__device__ __forceinline__ void st_row32(unsigned char *tile, int rows, int r, int c16, const uint32_t (&v)[8]) {
+    const int a = (c16 & 63) >> 3, sw = r & 7;
+    unsigned char *q = tile + (c16 >> 6) * rows * 128 + r * 128 + (((a ^ sw) & ~1) << 4);
+    if (sw & 1)
+        asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(q), "r"(v[4]), "r"(v[5]), "r"(v[6]),
+                     "r"(v[7]), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3])
+                     : "memory");
+    else
+        asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(q), "r"(v[0]), "r"(v[1]), "r"(v[2]),
+                     "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+                     : "memory");
+}
+
 __device__ __forceinline__ unsigned char *slot_of(const Ring &R, const Task &t) {
     return R.slots + static_cast<size_t>(t.k * RING + t.j % RING) * SLOT_BYTES;
 }
 
-// One task's inputs into shared memory, called by all threads once the input
-// tiles are free: 16-byte cp.async copies into the 128-byte-swizzled tile
-// layouts, g (fp32) in a first commit group, q, k, v (bf16) and beta (into
-// buffer bb) in a second, so the prefix sum can start before q, k and v land.
-// Rows past the sequence end are zero-filled (g = 0 keeps row 63 of G at the
-// last valid prefix; k = v = beta = 0 rows are inert in every product).
-__device__ __forceinline__ void issue_loads(const Params &p, unsigned char *smem, const Task &tk, int bb) {
-    const int tid = threadIdx.x;
+// One task's inputs into shared memory, issued by the `n` threads first ..
+// first + n - 1 once the input tiles are free: 16-byte cp.async copies into
+// the 128-byte-swizzled tile layouts, g (fp32) in a first commit group, q, k, v
+// (bf16) and beta (into buffer bb) in a second, so the prefix sum can start
+// before q, k and v land (every thread waits for its own groups, then the CTA
+// meets at a barrier). Rows past the sequence end are zero-filled (g = 0 keeps
+// row 63 of G at the last valid prefix; k = v = beta = 0 rows are inert in
+// every product).
+__device__ __forceinline__ void issue_loads(const Params &p, unsigned char *smem, const Task &tk, int bb, int first, int n) {
+    const int li = static_cast<int>(threadIdx.x) - first;
     const size_t rs = static_cast<size_t>(p.H) * DK;  // token stride, elements
     const size_t hb = static_cast<size_t>(tk.h) * DK;
-#pragma unroll
-    for (int it = 0; it < BT * 32 / NCOMP; ++it) {  // g: 64 rows x 32 chunks of 4 channels
-        const int idx = tid + it * NCOMP, r = idx >> 5, c4 = (idx & 31) << 2;
+    for (int idx = li; idx < BT * 32; idx += n) {  // g: 64 rows x 32 chunks of 4 channels
+        const int r = idx >> 5, c4 = (idx & 31) << 2;
         const bool ok = r < tk.nv;
         cp_async16(smem + OFF_G + g_chunk(r, c4), p.g + static_cast<size_t>(tk.t0 + (ok ? r : 0)) * rs + hb + c4,
                    ok ? 16 : 0);
     }
-    if (p.raw && tid < 33) {  // the gate activation's per-head parameters (zeros when not given)
-        if (tid < 32)
-            cp_async16(smem + OFF_GPAR + 16 * tid, p.dt_bias ? p.dt_bias + hb + 4 * tid : p.g, p.dt_bias ? 16 : 0);
+    if (p.raw && li < 33) {  // the gate activation's per-head parameters (zeros when not given)
+        if (li < 32)
+            cp_async16(smem + OFF_GPAR + 16 * li, p.dt_bias ? p.dt_bias + hb + 4 * li : p.g, p.dt_bias ? 16 : 0);
         else
             cp_async4(smem + OFF_GPAR + 512, p.A_log ? p.A_log + tk.h : p.g, p.A_log ? 4 : 0);
     }
     cp_async_commit();
-#pragma unroll
-    for (int it = 0; it < BT * 16 / NCOMP; ++it) {  // q, k, v: 64 rows x 16 chunks of 8 channels
-        const int idx = tid + it * NCOMP, r = idx >> 4, c8 = (idx & 15) << 3;
+    for (int idx = li; idx < BT * 16; idx += n) {  // q, k, v: 64 rows x 16 chunks of 8 channels
+        const int r = idx >> 4, c8 = (idx & 15) << 3;
         const bool ok = r < tk.nv;
         const size_t off = static_cast<size_t>(tk.t0 + (ok ? r : 0)) * rs + hb + c8;
         const int d = tile_chunk(64, r, c8);
@@ -511,8 +528,8 @@ __device__ __forceinline__ void issue_loads(const Params &p, unsigned char *smem
         cp_async16(smem + OFF_K + d, p.k + off, ok ? 16 : 0);
         cp_async16(smem + OFF_V + d, p.v + off, ok ? 16 : 0);
     }
-    if (tid >= NCOMP - BT) {  // warps 14 and 15
-        const int r = tid - (NCOMP - BT);
+    if (li >= n - BT) {  // the last 64 threads: beta
+        const int r = li - (n - BT);
         const bool ok = r < tk.nv;
         cp_async4(smem + OFF_BETA + 256 * bb + 4 * r, p.beta + static_cast<size_t>(tk.t0 + (ok ? r : 0)) * p.H + tk.h,
                   ok ? 4 : 0);
@@ -522,26 +539,149 @@ __device__ __forceinline__ void issue_loads(const Params &p, unsigned char *smem
 
 // The previous task's WY product X^T = [u | w]^T, read out of tensor memory
 // into the previous task's slot: u^T rows into U, w^T rows into atom column 1
-// of B1 (this thread: channel `chn`, tokens 16 blk .. 16 blk + 15).
-__device__ __forceinline__ void read_out_x(uint32_t tl, unsigned char *pd, int chn, int blk, float &vmax) {
-    uint32_t xu[16], xw[16];
-    tmem_ld16(tl + TM_XU + 16 * blk, xu);
-    tmem_ld16(tl + TM_XW + 16 * blk, xw);
-    tmem_wait_ld();
-    uint32_t u2[8], w2[8];
+// of B1 (this thread: channel `chn`, tokens 16 b .. 16 b + 15 for b in [b0, b1)).
+__device__ __forceinline__ void read_out_x(uint32_t tl, unsigned char *pd, int chn, int b0, int b1, float &vmax) {
+    for (int b = b0; b < b1; ++b) {
+        uint32_t xu[16], xw[16];
+        tmem_ld16(tl + TM_XU + 16 * b, xu);
+        tmem_ld16(tl + TM_XW + 16 * b, xw);
+        tmem_wait_ld();
+        uint32_t u2[8], w2[8];
+        float vm = vmax;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        const float a0 = __uint_as_float(xu[2 * e]), a1 = __uint_as_float(xu[2 * e + 1]);
-        const float b0 = __uint_as_float(xw[2 * e]), b1 = __uint_as_float(xw[2 * e + 1]);
-        vmax = max_abs_nan(max_abs_nan(vmax, a0), a1);
-        vmax = max_abs_nan(max_abs_nan(vmax, b0), b1);
-        u2[e] = pack_f16(a0, a1);
-        w2[e] = pack_f16(b0, b1);
+        for (int e = 0; e < 8; ++e) {
+            const float a0 = __uint_as_float(xu[2 * e]), a1 = __uint_as_float(xu[2 * e + 1]);
+            const float c0 = __uint_as_float(xw[2 * e]), c1 = __uint_as_float(xw[2 * e + 1]);
+            vm = max_abs_nan(max_abs_nan(vm, a0), a1);
+            vm = max_abs_nan(max_abs_nan(vm, c0), c1);
+            u2[e] = pack_f16(a0, a1);
+            w2[e] = pack_f16(c0, c1);
+        }
+        vmax = vm;
+        st_row32(pd + SL_U, 128, chn, 16 * b, u2);
+        st_row32(pd + SL_B1, 128, chn, 64 + 16 * b, w2);
     }
-    *reinterpret_cast<uint4 *>(pd + SL_U + tile_chunk(128, chn, 16 * blk)) = make_uint4(u2[0], u2[1], u2[2], u2[3]);
-    *reinterpret_cast<uint4 *>(pd + SL_U + tile_chunk(128, chn, 16 * blk + 8)) = make_uint4(u2[4], u2[5], u2[6], u2[7]);
-    *reinterpret_cast<uint4 *>(pd + SL_B1 + tile_chunk(128, chn, 64 + 16 * blk)) = make_uint4(w2[0], w2[1], w2[2], w2[3]);
-    *reinterpret_cast<uint4 *>(pd + SL_B1 + tile_chunk(128, chn, 72 + 16 * blk)) = make_uint4(w2[4], w2[5], w2[6], w2[7]);
+}
+
+// a slot's ready flag, released once the slot's contents have been written
+// (all of them ordered before this thread by a preceding barrier)
+__device__ __forceinline__ void publish(const Params &p, const Ring &R, const Task &t) {
+    fence_acq_rel_gpu();
+    if (!(p.debug & KDA_DEBUG_WITHHOLD_READY)) st_release(&R.ready[t.k * RING + t.j % RING], t.j + 1);
+}
+// whether task t's slot is free (its consumer has copied out the chunk that
+// used it RING chunks earlier), polling at most `polls` times
+__device__ __forceinline__ bool slot_free(const Ring &R, const Task &t, long long polls) {
+    if (t.j < RING) return true;
+    const int *f = &R.freed[t.k * RING + t.j % RING];
+    for (long long it = 0; it < polls; ++it) {
+        if (ld_acquire(f) >= t.j - RING + 1) return true;
+        __nanosleep(64);
+    }
+    return false;
+}
+
+// Step 2b for one group of strip tiles on one warp: row blocks R0 and R0 + 1
+// against column blocks C0 .. C0 + NC - 1 (the tiles (i, j) with j <= i among
+// them), so that each 16-channel step loads the A fragments of a row block and
+// the B values of a column block once for all the group's tiles. Aqk on tf32
+// (m16n8k8), Akk on bf16 (m16n8k16). Within each 16-channel step the tf32 k
+// slots are permuted (slot q <-> channel 2q, slot q+4 <-> channel 2q+1, for each
+// half) so that one 8-byte load of a k e^(G_m - G) row feeds both the tf32 and
+// the bf16 B fragments. Tile (i, j) needs k_s e^(G_{m_i} - G_s) for s in
+// sub-block j: the stored k e^(G_{m_j} - G) times e^(G_{m_i} - G_{m_j}) (<= 1).
+// Writes scale*Aqk into the slot and L = diag(beta) tril(Akk, -1) (and its
+// diagonal blocks in fp32) into shared memory.
+template <int R0, int C0, int NC>
+__device__ __forceinline__ void strip_group(const unsigned char *smem, unsigned char *dst, const float *sBeta, float scale,
+                                            int lane) {
+    const int gq = lane >> 2, qd = lane & 3;
+    const float *sKB = reinterpret_cast<const float *>(smem + OFF_KB);
+    const float *sF = reinterpret_cast<const float *>(smem + OFF_F);
+    __half *sL = reinterpret_cast<__half *>(const_cast<unsigned char *>(smem) + OFF_L);
+    float *sLD = reinterpret_cast<float *>(const_cast<unsigned char *>(smem) + OFF_LD);
+    float aq[2][NC][2][4], ak[2][NC][2][4];
+#pragma unroll
+    for (int ri = 0; ri < 2; ++ri)
+#pragma unroll
+        for (int cj = 0; cj < NC; ++cj)
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) aq[ri][cj][nt][e] = ak[ri][cj][nt][e] = 0.f;
+#pragma unroll 2
+    for (int kk = 0; kk < 8; ++kk) {
+        const int c0 = 16 * kk + 2 * qd;
+        uint32_t fa0[2][4], fa1[2][4], fk[2][4];
+#pragma unroll
+        for (int ri = 0; ri < 2; ++ri) {
+            const int i = R0 + ri;
+            const unsigned char *sQA = smem + OFF_QA;
+            const uint2 u00 = *reinterpret_cast<const uint2 *>(sQA + qa_pair(16 * i + gq, c0));
+            const uint2 u10 = *reinterpret_cast<const uint2 *>(sQA + qa_pair(16 * i + gq + 8, c0));
+            const uint2 u01 = *reinterpret_cast<const uint2 *>(sQA + qa_pair(16 * i + gq, c0 + 8));
+            const uint2 u11 = *reinterpret_cast<const uint2 *>(sQA + qa_pair(16 * i + gq + 8, c0 + 8));
+            fa0[ri][0] = u00.x; fa0[ri][1] = u10.x; fa0[ri][2] = u00.y; fa0[ri][3] = u10.y;
+            fa1[ri][0] = u01.x; fa1[ri][1] = u11.x; fa1[ri][2] = u01.y; fa1[ri][3] = u11.y;
+            ldsm_x4(fk[ri], smem + OFF_KA + a_addr(lane, 64, 16 * i, 16 * kk));
+        }
+        float2 x0[NC][2], x1[NC][2];
+#pragma unroll
+        for (int cj = 0; cj < NC; ++cj)
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const float *row = sKB + (16 * (C0 + cj) + 8 * nt + gq) * RSF;
+                x0[cj][nt] = *reinterpret_cast<const float2 *>(row + c0);
+                x1[cj][nt] = *reinterpret_cast<const float2 *>(row + c0 + 8);
+            }
+#pragma unroll
+        for (int ri = 0; ri < 2; ++ri)
+#pragma unroll
+            for (int cj = 0; cj < NC; ++cj) {
+                const int i = R0 + ri, j = C0 + cj;
+                if (j > i) continue;
+                float2 f0 = make_float2(1.f, 1.f), f1 = make_float2(1.f, 1.f);
+                if (i > j) {
+                    const float *fr = sF + f_pair(i, j) * 128;
+                    f0 = *reinterpret_cast<const float2 *>(fr + c0);
+                    f1 = *reinterpret_cast<const float2 *>(fr + c0 + 8);
+                }
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    const float b00 = x0[cj][nt].x * f0.x, b01 = x0[cj][nt].y * f0.y;
+                    const float b10 = x1[cj][nt].x * f1.x, b11 = x1[cj][nt].y * f1.y;
+                    mma1688_tf32(aq[ri][cj][nt], fa0[ri], tf32_rna(b00), tf32_rna(b01));
+                    mma1688_tf32(aq[ri][cj][nt], fa1[ri], tf32_rna(b10), tf32_rna(b11));
+                    mma16816(ak[ri][cj][nt], fk[ri], pack_bf16(b00, b01), pack_bf16(b10, b11));
+                }
+            }
+    }
+#pragma unroll
+    for (int ri = 0; ri < 2; ++ri)
+#pragma unroll
+        for (int cj = 0; cj < NC; ++cj) {
+            const int i = R0 + ri, j = C0 + cj;
+            if (j > i) continue;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    const int tl16 = gq + 8 * hf, sl = 8 * nt + 2 * qd;
+                    const int t = 16 * i + tl16, sc = 16 * j + sl;
+                    const float btt = sBeta[t];
+                    float vq[2], vk[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const bool incl = (i > j) || (sl + e <= tl16);
+                        const bool strict = (i > j) || (sl + e < tl16);
+                        vq[e] = incl ? scale * aq[ri][cj][nt][2 * hf + e] : 0.f;
+                        vk[e] = strict ? btt * ak[ri][cj][nt][2 * hf + e] : 0.f;
+                        if (i == j) sLD[(i * 16 + tl16) * 17 + sl + e] = vk[e];
+                    }
+                    *reinterpret_cast<uint32_t *>(dst + SL_B23 + tile_elem(192, 128 + t, sc)) = pack_f16(vq[0], vq[1]);
+                    *reinterpret_cast<uint32_t *>(sL + t * RSA + sc) = pack_f16(vk[0], vk[1]);
+                }
+        }
 }
 
 __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int pid) {
@@ -594,7 +734,8 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int pi
     Task cur = get_task(misc + 2);
     Task nxt = get_task(misc + 10);
     sync_compute();
-    if (cur.valid) issue_loads(p, smem, cur, 0);
+    if (cur.valid) issue_loads(p, smem, cur, 0, 0, NCOMP);
+    if (tid == REL_TID) misc[21] = cur.valid && slot_free(R, cur, R.spin) ? 1 : 0;  // nothing is unpublished yet
     const uint32_t idesc_x = umma_idesc_f16(false, false, 128, 64);  // R^T (tensor memory) x T^T (K-major)
     bool gate_bad = false;
     float vmax = 0.f;         // largest magnitude sent to an fp16 operand (NaN if any was NaN)
@@ -703,160 +844,125 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int pi
             tmem_st8(tl + TM_RK + 32 * bb + 8 * blk, rk);
             tmem_wait_st();
         }
+        const bool fast = misc[21] != 0;  // written during the previous task's strips
         tc_fence_before();
         sync_compute();  // input tiles consumed; strip operands and tables in place
         KDA_TRACE_EV(p, 21, 0);
-        if (tid == SYNC_TID) {
-            const Task t = fetch_task(p, smem, cu_s, jmax, cs);
-            put_task(misc + 2, t);
-        }
-        if (nxt.valid) issue_loads(p, smem, nxt, bb ^ 1);
-
-        // ---- the previous task's WY product: read out into its slot, then publish
-        if (x_pending) {
-            wait_local(R, bar_x, (it - 1) & 1, p.status);
-            tc_fence_after();
-            read_out_x(tl, slot_of(R, prev), chn, blk, vmax);
-            x_pending = false;
-        }
-        tc_fence_before();
-        sync_compute();  // every write of the previous slot issued; X^T read out
-        if (tid == REL_TID) {
-            if (prev.valid) {
-                fence_acq_rel_gpu();
-                if (!(p.debug & KDA_DEBUG_WITHHOLD_READY)) st_release(&R.ready[prev.k * RING + prev.j % RING], prev.j + 1);
+        // Is this task's slot known to be free (checked during the previous task)?
+        // If so, the previous task's WY product is read out and its slot published
+        // by warps 10-13 while the strips run. Otherwise every warp reads it out
+        // now, the slot is published, and only then is this task's slot awaited,
+        // so that no producer waits for a consumer while it holds an unpublished chunk.
+        if (!fast) {
+            if (x_pending) {
+                wait_local(R, bar_x, (it - 1) & 1, p.status);
+                tc_fence_after();
+                read_out_x(tl, slot_of(R, prev), chn, blk, blk + 1, vmax);
+                x_pending = false;
             }
-            const int s = cur.j % RING;
-            const bool free_ok =
-                (cur.j < RING) || wait_flag_geq(R, &R.freed[cur.k * RING + s], cur.j - RING + 1, p.status);
-            misc[20] = free_ok ? 1 : 0;
+            tc_fence_before();
+            sync_compute();  // every write of the previous slot issued; X^T read out
+            if (tid == REL_TID) {
+                if (prev.valid) publish(p, R, prev);
+                const bool ok = slot_free(R, cur, R.spin);
+                if (!ok) {
+                    set_status(p.status, KDA_ERR_TIMEOUT);
+                    atomicExch(&R.hdr->abort, 1);
+                }
+                misc[20] = ok ? 1 : 0;
+            }
+            sync_compute();
+            if (!misc[20]) break;
+            prev.valid = 0;
         }
-        sync_compute();
-        const Task nxt2 = get_task(misc + 2);
-        if (!misc[20]) break;
         KDA_TRACE_EV(p, 22, 0);
         unsigned char *dst = slot_of(R, cur);
-        *reinterpret_cast<uint4 *>(dst + SL_B1 + tile_chunk(128, chn, 16 * blk)) = make_uint4(qh[0], qh[1], qh[2], qh[3]);
-        *reinterpret_cast<uint4 *>(dst + SL_B1 + tile_chunk(128, chn, 16 * blk + 8)) = make_uint4(qh[4], qh[5], qh[6], qh[7]);
-        *reinterpret_cast<uint4 *>(dst + SL_B23 + tile_chunk(192, chn, 16 * blk)) =
-            make_uint4(kgp[0], kgp[1], kgp[2], kgp[3]);
-        *reinterpret_cast<uint4 *>(dst + SL_B23 + tile_chunk(192, chn, 16 * blk + 8)) =
-            make_uint4(kgp[4], kgp[5], kgp[6], kgp[7]);
+        st_row32(dst + SL_B1, 128, chn, 16 * blk, qh);
+        st_row32(dst + SL_B23, 192, chn, 16 * blk, kgp);
         if (blk == 0) reinterpret_cast<float *>(dst + SL_D)[chn] = ex2(Gl);
 
-        // ---- step 2b: Aqk (tf32) and Akk (bf16) on the 10 lower 16x16 tiles,
-        // one tile per warp. Tile (i,j) needs k_s e^(G_{m_i} - G_s) for s in
-        // sub-block j: the stored k e^(G_{m_j} - G) times e^(G_{m_i} - G_{m_j}) (<= 1).
-        static_assert(NWARPS == 16, "warps 0-9 strips, 10, 11, 14, 15 diagonal inverses, 12-13 zero tiles");
-        // Warp w runs on sub-partition w % 4, so warps 0-9 leave partitions 0 and 1
-        // with three tiles and 2 and 3 with two: the diagonal tiles (pairs 0, 2, 5,
-        // 9), whose L_ii feed the inverses, go to warps 2, 3, 6, 7 on the lighter ones.
-        if (warp < 10) {
-            const int pair = (0x8795642031ull >> (4 * warp)) & 15;  // warp -> pair: 1 3 0 2 4 6 5 9 7 8
-            int i = 0;
-            while ((i + 1) * (i + 2) / 2 <= pair) ++i;
-            const int j = pair - i * (i + 1) / 2;
-            const float *kbrow0 = sKB + (16 * j + gq) * RSF;      // column s = 16j + gq
-            const float *kbrow1 = sKB + (16 * j + 8 + gq) * RSF;  // column s = 16j + 8 + gq
-            const float *fr = sF + (i > j ? f_pair(i, j) : 0) * 128;
-            float aq[2][4] = {}, ak[2][4] = {};
-            // Aqk on tf32 (m16n8k8), Akk on bf16 (m16n8k16). Within each 16-channel
-            // step the tf32 k slots are permuted (slot q <-> channel 2q, slot q+4 <->
-            // channel 2q+1, for each half) so that one 8-byte load of the scaled
-            // k row feeds both the tf32 and the bf16 B fragments.
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const int c0 = 16 * kk + 2 * qd;
-                uint32_t fa0[4], fa1[4], fk[4];
-                {
-                    const unsigned char *sQA = smem + OFF_QA;
-                    const uint2 u00 = *reinterpret_cast<const uint2 *>(sQA + qa_pair(16 * i + gq, c0));
-                    const uint2 u10 = *reinterpret_cast<const uint2 *>(sQA + qa_pair(16 * i + gq + 8, c0));
-                    const uint2 u01 = *reinterpret_cast<const uint2 *>(sQA + qa_pair(16 * i + gq, c0 + 8));
-                    const uint2 u11 = *reinterpret_cast<const uint2 *>(sQA + qa_pair(16 * i + gq + 8, c0 + 8));
-                    fa0[0] = u00.x; fa0[1] = u10.x; fa0[2] = u00.y; fa0[3] = u10.y;
-                    fa1[0] = u01.x; fa1[1] = u11.x; fa1[2] = u01.y; fa1[3] = u11.y;
-                }
-                ldsm_x4(fk, smem + OFF_KA + a_addr(lane, 64, 16 * i, 16 * kk));
-                float2 f0 = make_float2(1.f, 1.f), f1 = make_float2(1.f, 1.f);
-                if (i > j) {
-                    f0 = *reinterpret_cast<const float2 *>(fr + c0);
-                    f1 = *reinterpret_cast<const float2 *>(fr + c0 + 8);
-                }
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    const float *row = nt ? kbrow1 : kbrow0;
-                    const float2 x0 = *reinterpret_cast<const float2 *>(row + c0);
-                    const float2 x1 = *reinterpret_cast<const float2 *>(row + c0 + 8);
-                    const float b00 = x0.x * f0.x, b01 = x0.y * f0.y, b10 = x1.x * f1.x, b11 = x1.y * f1.y;
-                    mma1688_tf32(aq[nt], fa0, tf32_rna(b00), tf32_rna(b01));
-                    mma1688_tf32(aq[nt], fa1, tf32_rna(b10), tf32_rna(b11));
-                    mma16816(ak[nt], fk, pack_bf16(b00, b01), pack_bf16(b10, b11));
-                }
-            }
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    const int tl16 = gq + 8 * hf, sl = 8 * nt + 2 * qd;
-                    const int t = 16 * i + tl16, s = 16 * j + sl;
-                    const float btt = sBeta[t];
-                    float vq[2], vk[2];
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const bool incl = (i > j) || (sl + e <= tl16);
-                        const bool strict = (i > j) || (sl + e < tl16);
-                        vq[e] = incl ? scale * aq[nt][2 * hf + e] : 0.f;
-                        vk[e] = strict ? btt * ak[nt][2 * hf + e] : 0.f;
-                        if (i == j) sLD[(i * 16 + tl16) * 17 + sl + e] = vk[e];
-                    }
-                    *reinterpret_cast<uint32_t *>(dst + SL_B23 + tile_elem(192, 128 + t, s)) = pack_f16(vq[0], vq[1]);
-                    *reinterpret_cast<uint32_t *>(sL + t * RSA + s) = pack_f16(vk[0], vk[1]);
-                }
-            if (i == j) {  // L_ii is in place: hand it to the inverse warp of block i
+        // ---- step 2b: Aqk and Akk on the 10 lower 16x16 tiles in four groups,
+        // warps 0-3 (one per sub-partition): rows {0,1} x columns {0,1},
+        // rows {2,3} x column 0, rows {2,3} x column 1, rows {2,3} x columns {2,3}
+        static_assert(NWARPS == 16, "warps 0-3 strips, 4-9 next inputs, 10-13 WY read-out, 14-15 diagonal inverses");
+        if (warp < 4) {
+            if (warp == 0) strip_group<0, 0, 2>(smem, dst, sBeta, scale, lane);
+            else if (warp == 1) strip_group<2, 0, 1>(smem, dst, sBeta, scale, lane);
+            else if (warp == 2) strip_group<2, 1, 1>(smem, dst, sBeta, scale, lane);
+            else strip_group<2, 2, 2>(smem, dst, sBeta, scale, lane);
+            if (warp == 0 || warp == 3) {  // the diagonal blocks of L are in place: hand them to the inverse warps
                 __syncwarp();
-                named_bar_arrive(2 + i, 64);
+                named_bar_arrive(2, 128);
             }
             if (lane == 0) KDA_TRACE_ANY(p, 40 + warp, 0);
         }
-        // ---- step 3a, on warps 10, 11, 14, 15 (blocks 0-3) while the strips run:
-        // T_ii = (I + L_ii)^-1 by fp32 forward substitution, once the warp with
-        // tile (i, i) has written L_ii
-        if (warp == 10 || warp == 11 || warp == 14 || warp == 15) {
-            const int i = (warp & 1) | ((warp & 4) >> 1);
-            named_bar_sync(2 + i, 64);
-            if (lane < 16) {
-                const int jc = lane;
-                const float *Ld = sLD + i * 16 * 17;
-                float x[16];
-#pragma unroll
-                for (int r = 0; r < 16; ++r) {
-                    float s = (r == jc) ? 1.f : 0.f;
-#pragma unroll
-                    for (int cc = 0; cc < r; ++cc) s -= Ld[r * 17 + cc] * x[cc];
-                    x[r] = s;
-                }
-                float vm = 0.f;
-#pragma unroll
-                for (int r = 0; r < 16; ++r) {
-                    vm = max_abs_nan(vm, x[r]);
-                    *reinterpret_cast<__half *>(sT + tile_elem(64, 16 * i + r, 16 * i + jc)) = __float2half_rn(x[r]);
-                }
-                vmax = max_abs_nan(vmax, vm);
+        // ---- warps 4-9: the next task's inputs (the input tiles are free) and its draw
+        if (warp >= 4 && warp < 10) {
+            if (tid == SYNC_TID) {
+                const Task t = fetch_task(p, smem, cu_s, jmax, cs);
+                put_task(misc + 2, t);
             }
-            if (lane == 0) KDA_TRACE_ANY(p, 50 + i, 0);
+            if (nxt.valid) issue_loads(p, smem, nxt, bb ^ 1, 4 * 32, 6 * 32);
         }
-        // ---- warps 12 and 13: the six tiles of scale*Aqk above the diagonal are zero
-        if (warp == 12 || warp == 13) {
-            for (int idx = tid - 12 * 32; idx < 6 * 16 * 2; idx += 64) {
-                const int tile = idx >> 5, rr = (idx >> 1) & 15, half = idx & 1;
-                const int i = tile < 3 ? 0 : (tile < 5 ? 1 : 2);
-                const int j = tile < 3 ? tile + 1 : (tile < 5 ? tile - 1 : 3);
-                *reinterpret_cast<uint4 *>(dst + SL_B23 + tile_chunk(192, 128 + 16 * i + rr, 16 * j + 8 * half)) =
-                    make_uint4(0, 0, 0, 0);
+        // ---- step 3a, on warps 14 and 15 (two blocks each, 16 lanes per block)
+        // while the strips run: T_ii = (I + L_ii)^-1 by fp32 forward substitution,
+        // once the four warps with the diagonal tiles have written them
+        if (warp >= 14) {
+            named_bar_sync(2, 128);
+            const int i = 2 * (warp - 14) + (lane >> 4), jc = lane & 15;
+            const float *Ld = sLD + i * 16 * 17;
+            float x[16];
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+                float sacc = (r == jc) ? 1.f : 0.f;
+#pragma unroll
+                for (int cc = 0; cc < r; ++cc) sacc -= Ld[r * 17 + cc] * x[cc];
+                x[r] = sacc;
+            }
+            float vm = 0.f;
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+                vm = max_abs_nan(vm, x[r]);
+                *reinterpret_cast<__half *>(sT + tile_elem(64, 16 * i + r, 16 * i + jc)) = __float2half_rn(x[r]);
+            }
+            vmax = max_abs_nan(vmax, vm);
+            if (lane == 0) KDA_TRACE_ANY(p, 50 + warp - 14, 0);
+        }
+        // ---- warps 10-13 (one per lane quarter): the previous task's WY product
+        // into its slot, then its publication; and whether the next task's slot
+        // is free: one flag load, issued first and completed by the publication's
+        // fence (an acquire), so that nothing here waits on a consumer
+        if (warp >= 10 && warp < 14) {
+            const bool need_check = nxt.valid && nxt.j >= RING;
+            int fr = 0;
+            if (tid == REL_TID && need_check) fr = ld_relaxed(&R.freed[nxt.k * RING + nxt.j % RING]);
+            if (x_pending) {
+                wait_local(R, bar_x, (it - 1) & 1, p.status);
+                tc_fence_after();
+                read_out_x(tl, slot_of(R, prev), chn, 0, 4, vmax);
+            }
+            if (cur.j < RING) {  // the first use of this slot: the tiles of Aqk above the diagonal are zero
+                for (int idx = tid - 10 * 32; idx < 6 * 16 * 2; idx += 128) {
+                    const int tile = idx >> 5, rr = (idx >> 1) & 15, half = idx & 1;
+                    const int i = tile < 3 ? 0 : (tile < 5 ? 1 : 2);
+                    const int j = tile < 3 ? tile + 1 : (tile < 5 ? tile - 1 : 3);
+                    *reinterpret_cast<uint4 *>(dst + SL_B23 + tile_chunk(192, 128 + 16 * i + rr, 16 * j + 8 * half)) =
+                        make_uint4(0, 0, 0, 0);
+                }
+            }
+            named_bar_sync(6, 128);
+            if (tid == REL_TID) {
+                if (x_pending && prev.valid)
+                    publish(p, R, prev);
+                else if (need_check)
+                    fence_acq_rel_gpu();
+                misc[21] = (nxt.valid && (!need_check || fr >= nxt.j - RING + 1)) ? 1 : 0;
+                KDA_TRACE_ANY(p, 29, 0);
             }
         }
         sync_compute();
+        x_pending = false;
+        const Task nxt2 = get_task(misc + 2);  // drawn after the elementwise step
         KDA_TRACE_EV(p, 23, 0);
 
         // ---- step 3b: the block diagonals d = 1, 2, 3 of T = (I + L)^-1,
@@ -934,13 +1040,10 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int pi
     if (x_pending) {
         wait_local(R, bar_x, (it - 1) & 1, p.status);
         tc_fence_after();
-        read_out_x(tl, slot_of(R, prev), chn, blk, vmax);
+        read_out_x(tl, slot_of(R, prev), chn, blk, blk + 1, vmax);
         tc_fence_before();
         sync_compute();
-        if (tid == REL_TID) {
-            fence_acq_rel_gpu();
-            if (!(p.debug & KDA_DEBUG_WITHHOLD_READY)) st_release(&R.ready[prev.k * RING + prev.j % RING], prev.j + 1);
-        }
+        if (tid == REL_TID) publish(p, R, prev);
     }
     cp_async_wait_all();
     if (gate_bad) set_status(p.status, KDA_ERR_GATE_RANGE);
@@ -996,7 +1099,8 @@ __device__ __forceinline__ uint32_t sigmoid_bf16x2_to_f16x2(uint32_t g2) {
 // T(l)), then over the four column quarters in shared memory; called by all
 // threads together (it holds two CTA barriers).
 __device__ __forceinline__ void store_o(const Params &p, unsigned char *smem, const uint32_t (&ov)[16], int64_t t0, int nv,
-                                        int h, int jv, int cg, int lane, int quad, const uint32_t (&gt)[8], float nw) {
+                                        int h, int jv, int cg, int lane, int quad, const uint32_t (&gt)[8], float nw,
+                                        int e0 = 0, int e1 = 16) {
     const int tid = threadIdx.x;
     float x[16];
 #pragma unroll
@@ -1040,7 +1144,7 @@ __device__ __forceinline__ void store_o(const Params &p, unsigned char *smem, co
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
             const int t = 16 * cg + e;
-            if (t < nv) p.o[(static_cast<size_t>(t0 + t) * p.H + h) * DV + jv] = x[e];
+            if (e >= e0 && e < e1 && t < nv) p.o[(static_cast<size_t>(t0 + t) * p.H + h) * DV + jv] = x[e];
         }
     }
 }
@@ -1229,8 +1333,12 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
                 tmem_st16(tl + TM_S + 32 * cg, sa);
                 tmem_st16(tl + TM_S + 32 * cg + 16, sb);
             }
-            if (pend) store_o(p, smem, ov, pt0, pnv, ph, jv, cg, lane, quad, gt, nw);
+            KDA_TRACE_EV(p, 15, jj);
+            // the first half of the previous chunk's o rows (the other half is stored
+            // while MMA23 runs; with the gated norm all of them are, then)
+            if (pend && !p.ngate) store_o(p, smem, ov, pt0, pnv, ph, jv, cg, lane, quad, gt, nw, 0, 8);
             tmem_wait_st();
+            KDA_TRACE_EV(p, 16, jj);
 
             // (5) E2: v_new^T = u^T - (w S)^T -> fp16 A operand of MMA23
             wait_local(R, bar_mma1, jj & 1, p.status);
@@ -1268,6 +1376,7 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
                     umma_f16_ts(tmem + TM_S, tmem + TM_VN + 8 * kk, umma_desc_sw128(b23 + kk * 32, 16, 1024), idesc23, 1);
                 umma_commit(bar_mma23);
             }
+            if (pend) store_o(p, smem, ov, pt0, pnv, ph, jv, cg, lane, quad, gt, nw, p.ngate ? 0 : 8, 16);
             ++n23;
             pend = true;
             pt0 = t0;
