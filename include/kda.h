@@ -56,8 +56,11 @@ typedef enum {
     KDA_ERR_TIMEOUT = 6,     /* device: a bounded wait inside a kernel gave up */
     KDA_ERR_VALUE_RANGE = 7, /* device: a value entering an fp16 tensor-core operand
                                 exceeded 6e4 in magnitude (or was not finite) */
-    KDA_ERR_SCRATCH_TOO_SMALL = 8 /* kda_chunk_fwd_static_scratch: the problem needs more
-                                     scratch than KDA_STATIC_SCRATCH_BYTES */
+    KDA_ERR_SCRATCH_TOO_SMALL = 8, /* kda_chunk_fwd_static_scratch: the problem needs more
+                                      scratch than KDA_STATIC_SCRATCH_BYTES */
+    KDA_ERR_BOUNDS = 9 /* device, only in a library compiled with -DKDA_DEBUG_BOUNDS: an
+                          index checked before a global-memory access fell outside its
+                          buffer; that access was skipped (no trap) */
 } kda_status_t;
 
 #define KDA_HEAD_DIM 128

@@ -25,6 +25,7 @@ KDA_ERR_BAD_SEQLENS = 5
 KDA_ERR_TIMEOUT = 6
 KDA_ERR_VALUE_RANGE = 7
 KDA_ERR_SCRATCH_TOO_SMALL = 8
+KDA_ERR_BOUNDS = 9
 KDA_DEBUG_WITHHOLD_READY = 1
 
 HEAD_DIM = 128

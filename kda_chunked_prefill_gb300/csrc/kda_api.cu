@@ -196,6 +196,7 @@ const char *kda_status_string(int32_t status) {
         case KDA_ERR_TIMEOUT: return "a bounded wait inside a kernel gave up";
         case KDA_ERR_VALUE_RANGE: return "a value entering an fp16 tensor-core operand exceeded 6e4 or was not finite";
         case KDA_ERR_SCRATCH_TOO_SMALL: return "problem needs more scratch than the static scratch array holds";
+        case KDA_ERR_BOUNDS: return "an index checked before a global-memory access was out of bounds (KDA_DEBUG_BOUNDS build)";
         default: return "unknown status";
     }
 }

@@ -120,6 +120,20 @@ __device__ __forceinline__ void set_status(int32_t *status, int32_t code) {
     if (status) atomicCAS(status, 0, code);
 }
 
+// Index check before a global-memory access. In a library compiled with
+// -DKDA_DEBUG_BOUNDS a false `ok` records KDA_ERR_BOUNDS (9, as in kda.h) and
+// the caller skips the access; other builds compile the check away.
+__device__ __forceinline__ bool checked(bool ok, int32_t *status) {
+#ifdef KDA_DEBUG_BOUNDS
+    if (!ok) set_status(status, 9);
+    return ok;
+#else
+    (void)ok;
+    (void)status;
+    return true;
+#endif
+}
+
 // ---- release / acquire flags in global memory (gpu scope)
 __device__ __forceinline__ int ld_acquire(const int *p) {
     int v;
@@ -250,35 +264,5 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-
-// 8 consecutive 32-bit columns of this thread's TMEM lane
-__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
-                 : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
-                 "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]));
-}
-// tcgen05.mma kind::f16 with the A operand in tensor memory (row m in lane m;
-// column c holds the 16-bit elements 2c (low half) and 2c + 1 (high half) of the row)
-__device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
-                                            uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate));
-}
-// max of a and |b| that returns NaN when either is NaN (so a running maximum
-// of magnitudes also flags NaN inputs)
-__device__ __forceinline__ float max_abs_nan(float a, float b) {
-    float r;
-    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(fabsf(b)));
-    return r;
-}
-// orders this thread's earlier memory accesses (and, through a preceding CTA
-// barrier, its block's) before its later ones at GPU scope
-__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
 }  // namespace kda

@@ -1,23 +1,20 @@
 // KDA chunked prefill forward — persistent cooperative kernel, one CTA per SM,
 // in two roles that hand chunks to each other through a small ring in L2.
 //
-//   producers  run the intra-chunk steps of "在 TPU 上加速 Kimi K3 KDA" (junyi.dev
-//              tpu-kda report) for (chain, chunk) tasks: step 1 gate prefix sum
-//              (§6.1), step 2 Aqk/Akk as products of sub-block-midpoint-rescaled
-//              operands (§4), step 3 T = (I+L)^-1 by 16x16 blocks, step 4 the WY
-//              form [u | w] = T [beta v | beta k e^G] on the 5th-generation tensor
-//              cores, plus q_hat = scale q e^G and kg = k e^(G_last - G) (§4,
-//              §6.3). One thread owns one key channel of one 16-token sub-block,
-//              so the prefix sum runs in registers and every per-channel product
-//              leaves as a contiguous row of the ring slot, in the layouts the
-//              consumer's tensor-core operands use; then the slot's ready flag is
-//              released.
+//   producers  pull (chain, chunk) tasks from a global counter and run the
+//              intra-chunk steps of "在 TPU 上加速 Kimi K3 KDA" (junyi.dev
+//              tpu-kda report): step 1 gate prefix sum (§6.1), step 2 Aqk/Akk
+//              as products of sub-block-midpoint-rescaled operands (§4), step 3
+//              (I+L)^-1 by 16x16 block forward substitution, step 4 the WY form
+//              u, w plus q_hat = scale q e^G and kg = k e^(G_last - G) (§4, §6.3).
+//              They write [q_hat; w], kg, u, scale*Aqk and d = e^(G_last) into a
+//              ring slot already in the swizzled layouts the consumer's tensor-
+//              core operands use, then release the slot's ready flag.
 //   consumers  own (sequence, head) chains and run step 5 chunk after chunk
-//              (§6.2) on the transposed state S^T (tensor-memory lane = value
-//              column): D^T = S^T [q_hat; w]^T, v_new^T = u^T - (w S)^T,
-//              S^T <- S^T Diag(d) and [S^T | o^T] += v_new^T [kg | Aqk^T] in one
-//              product, reading the entry state; both per-chunk A operands stay in
-//              tensor memory, and each o row leaves as coalesced stores.
+//              (§6.2): v_new = u - w S, o = q_hat S + Aqk v_new,
+//              S <- Diag(d) S + kg^T v_new, reading the entry state, with the
+//              state on chip for the whole chain; each slot is streamed into
+//              shared memory by a bulk copy issued one chunk ahead.
 //
 // The chunk-to-chunk dependency of a chain is the only serial part; the
 // intra-chunk work (most of the arithmetic) is spread over every other SM.
@@ -41,20 +38,17 @@ constexpr int TRACE_COUNTS_OFFSET = 231424;  // past every role's tiles (checked
 #endif
 
 // ---------------------------------------------------------------- slot layout
-// A slot holds one (chain, chunk) hand-off in the shared-memory layouts of the
-// consumer's tensor-core operands; every region is 1024-byte aligned.
-//   B1   [q_hat ; w]^T  fp16 [key][token], MN-major: atom column 0 holds the
-//                       64 tokens of q_hat, atom column 1 those of w (32 KB)
-//   B23  [kg^T ; Aqk]   fp16, K-major rows of 64 tokens: rows 0-127 are key
-//                       channels (kg^T[c][s]), rows 128-191 tokens t
-//                       (scale * Aqk[t][s], zero above the diagonal) (24 KB)
-//   U    u^T            fp16 [value][token] (16 KB)
-//   D    e^(G_last)     fp32 [128]
+// A slot holds one (chain, chunk) hand-off; every region is 1024-byte aligned.
+//   A1  [q_hat ; w]  fp16, 128 rows x 128 key channels, K-major, 128B swizzle
+//   KG  kg           fp16, [token][key] (64 x 128): the transposed operand kg^T
+//   U   u            fp16, [token][value] (64 x 128)
+//   D   e^(G_last)   fp32, 128
+//   AQK scale * Aqk  fp16, [t][s] (64 x 64), causal incl. diagonal
 // 128-byte swizzle: row r of a 128-byte-wide atom column keeps its 16-byte
 // chunk c at position c ^ (r mod 8); wider tiles are split into 64-element
 // atom columns stored one after the other.
-constexpr int SL_B1 = 0, SL_B23 = 32768, SL_U = 57344, SL_D = 73728;
-static_assert(SLOT_BYTES == 74752 && SL_D + 512 <= SLOT_BYTES, "slot size");
+constexpr int SL_A1 = 0, SL_KG = 32768, SL_U = 49152, SL_D = 65536, SL_AQK = 66560;
+static_assert(SLOT_BYTES == 74752, "slot size");
 
 __device__ __forceinline__ int swz(int r, int chunk) { return (chunk ^ (r & 7)) << 4; }
 // byte offset of the 16-byte chunk holding columns [c8, c8+8) of row r of a
@@ -206,7 +200,7 @@ constexpr int SCHED_CU = 16 + 4 * (SCHED_MAX_C + 1) + 4 * SCHED_MAX_CHAINS;  // 
 constexpr int SCHED_BYTES = SCHED_CU + 4 * CU_CACHE;
 // The schedule sits at OFF_SCHED of every CTA's shared memory, past both roles'
 // tiles: int flags[4] (table present, cu copy present), cstart, order, cu copy.
-constexpr int OFF_SCHED = 197632;  // past both roles' tiles (checked below)
+constexpr int OFF_SCHED = 215168;  // = the consumer's tiles, the larger role (checked below)
 __device__ __forceinline__ const int *sched_flags(const unsigned char *smem) {
     return reinterpret_cast<const int *>(smem + OFF_SCHED);
 }
@@ -359,27 +353,13 @@ __device__ __forceinline__ bool map_task(const Params &p, const unsigned char *s
     }
 }
 
-// completion of this CTA's own tensor-core products: depends on no other CTA,
-// so only a (bounded) timeout ends it early, never the abort word
-__device__ __forceinline__ bool wait_local(const Ring &R, uint64_t *bar, uint32_t parity, int32_t *status) {
-    for (long long it = 0; it < SPIN_LIMIT; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-    }
-    set_status(status, KDA_ERR_TIMEOUT);
-    atomicExch(&R.hdr->abort, 1);
-    return false;
-}
-
 // ================================================================== producer
-// Steps 1-4 for one (chain, chunk) task at a time on all sixteen warps. Warp w
-// owns key channels 32 (w % 4) .. 32 (w % 4) + 31 (its tensor-memory lane
-// quarter) of sub-block w / 4, one channel per thread, for the prefix sum, the
-// elementwise products, the tensor-memory operand R^T and the read-out of the
-// WY product. The strips run on warp-level tensor-core products (m16n8k8 tf32,
-// m16n8k16 bf16) over the ten lower 16x16 tiles, the WY product on tcgen05
-// with its A operand in tensor memory. The WY product of a task is read out
-// during the next task (after its elementwise step), and the task's slot is
-// published right then, before the producer waits for anything else.
+// Steps 1-4 for one (chain, chunk) task at a time on all sixteen warps, with
+// warp-level tensor-core products (m16n8k16) for the 16x16 tiles. The task's
+// ring slot is assembled in shared memory (the slot image) and leaves with one
+// bulk store; while warps 0-9 compute the strips, one thread of the idle last
+// warp publishes the previous slot, draws the next task and waits for this
+// task's slot to be free, so none of that memory traffic stalls the warps.
 // Round an fp32 value to tf32 (nearest, ties away from zero) for a tf32 MMA
 // operand: adding half a tf32 unit in the last place to the sign-magnitude bit
 // pattern carries into bit 13 exactly when the dropped 13 bits are at least
@@ -387,37 +367,36 @@ __device__ __forceinline__ bool wait_local(const Ring &R, uint64_t *bar, uint32_
 __device__ __forceinline__ uint32_t tf32_rna(float x) { return __float_as_uint(x) + 0x1000u; }
 
 namespace prod {
+// q, k, v and their derived tiles are [64 tokens][128 channels] 16-bit tiles
+// and g is a [64][128] fp32 tile, all in the 128-byte-swizzled layout the
+// input copies write (16 KB and 32 KB; 1024-byte aligned).
 constexpr int RSF = 136, RSA = 72;
-constexpr int SZ_T = BT * DK * 2;                   // 16384: one [64][128] 16-bit tile
-constexpr int OFF_Q = 0, OFF_K = SZ_T, OFF_V = 2 * SZ_T;  // q, k, v (bf16, tile layout)
-constexpr int OFF_G = 3 * SZ_T;                     // g (fp32, g_chunk layout, 32 KB)
-constexpr int OFF_QA = OFF_G + 2 * SZ_T;            // q e^(G - G_m) as tf32 (fp32 words, qa_pair layout, 32 KB)
-constexpr int OFF_KA = OFF_QA + 2 * SZ_T;           // k e^(G - G_m) (bf16, tile layout)
-constexpr int OFF_KB = OFF_KA + SZ_T;               // k e^(G_m - G) (fp32 [64][RSF])
-constexpr int OFF_L = OFF_KB + BT * RSF * 4;        // L = diag(beta) tril(Akk, -1) (fp16 [64][RSA])
-constexpr int OFF_LD = OFF_L + BT * RSA * 2;        // diagonal blocks of L (fp32 [4][16][17])
-constexpr int OFF_T = (OFF_LD + 4352 + 1023) / 1024 * 1024;  // T = (I+L)^-1 (fp16 [t][s], tile layout, 64 rows)
-constexpr int OFF_GM = OFF_T + 8192;                // G at the sub-block midpoints (fp32 [4][128])
-constexpr int OFF_TOT = OFF_GM + 2048;              // per-sub-block sums of g, base 2 (fp32 [4][128])
-constexpr int OFF_F = OFF_TOT + 2048;               // 2^(G_mi - G_mj) for j < i (fp32 [6][128])
-constexpr int OFF_BETA = OFF_F + 3072;              // beta, two buffers of 64 fp32
-constexpr int OFF_MISC = OFF_BETA + 512;            // flags and the task broadcast (32 ints)
-constexpr int OFF_GPAR = OFF_MISC + 128;            // raw gates: the task head's dt_bias row (128 fp32) and A_log
-constexpr int OFF_BAR = OFF_GPAR + 528;             // WY-product mbarrier, then the TMEM base address
-constexpr int SMEM = OFF_BAR + 16;
-static_assert(OFF_GPAR % 16 == 0 && OFF_BAR % 8 == 0, "alignment");
-static_assert(OFF_Q % 1024 == 0 && OFF_G % 1024 == 0 && OFF_KA % 1024 == 0 && OFF_T % 1024 == 0,
-              "swizzled tiles are 1024-byte aligned");
-// Tensor memory: R^T = [beta v | beta k e^G]^T (fp16, lane = channel, column c
-// = tokens 2c and 2c + 1) in two buffers at +32 columns, and the WY product
-// X^T = [u | w]^T (fp32, lane = channel, column = token).
-constexpr uint32_t TM_RV = 0, TM_RK = 64, TM_XU = 128, TM_XW = 192, TM_COLS = 256;
+constexpr int SZ_T = BT * DK * 2;             // 16384
+constexpr int SZ_F = BT * RSF * 4;            // 34816 (kb keeps a padded row stride)
+constexpr int OFF_IMG = 0;                    // slot image: the bytes of one ring slot
+constexpr int OFF_Q = OFF_IMG + SLOT_BYTES;   // q; then q*a as tf32 (fp32 [64][128], spans OFF_Q and OFF_QLO)
+constexpr int OFF_QLO = OFF_Q + SZ_T;
+constexpr int OFF_K = OFF_QLO + SZ_T;         // k -> k*a (bf16)
+constexpr int OFF_V = OFF_K + SZ_T;           // v (bf16)
+constexpr int OFF_GKB = OFF_V + SZ_T;         // g -> G (fp32, swizzled), then k*e^(G_m - G) (fp32, padded)
+constexpr int SZ_A = BT * RSA * 2;            // 9216
+constexpr int OFF_L = OFF_GKB + SZ_F;         // L (fp16 [64][RSA])
+constexpr int OFF_LD = OFF_L + SZ_A;          // diagonal blocks of L, fp32 [4][16][17]
+constexpr int OFF_T = OFF_LD + 4352;          // T = (I+L)^-1, fp16 [64][RSA] (lower blocks)
+constexpr int OFF_TAB = OFF_T + SZ_A;         // per-channel tables, fp32 [20][128]
+constexpr int OFF_BETA = OFF_TAB + 10240;
+constexpr int OFF_MISC = OFF_BETA + 256;      // flags and the task broadcast (32 ints)
+constexpr int OFF_GPAR = OFF_MISC + 128;      // raw gates: the task head's dt_bias row (128 fp32) and A_log
+constexpr int SMEM = OFF_GPAR + 528;
+static_assert(OFF_GPAR % 16 == 0, "cp.async destinations are 16-byte aligned");
 // Warp w runs on sub-partition w % 4. During the strips, warps 0-9 hold the
 // ten tiles (three on partitions 0 and 1, two on 2 and 3); the diagonal
-// inverses run on warps 10, 11, 14, 15 (partitions 2 and 3) and the zero tiles
-// of Aqk on warps 12 and 13 (partitions 0 and 1).
-constexpr int SYNC_TID = 9 * 32;              // lane 0 of warp 9: draws tasks
-constexpr int REL_TID = 12 * 32;              // lane 0 of warp 12: publishes slots, waits for free slots
+// inverses run on warps 10, 11, 14, 15 (partitions 2 and 3) and the ring work,
+// mostly waiting, on warps 12 and 13 (partitions 0 and 1).
+constexpr int SYNC_TID = 13 * 32;             // lane 0 of warp 13: draws tasks
+constexpr int REL_TID = 12 * 32;              // lane 0 of warp 12: waits for free slots, stores and publishes images
+constexpr int TGM = 0, TGL = 4 * 128, TEM = 5 * 128, TEL = 9 * 128, TF = 13 * 128, TD = 19 * 128;
+static_assert(OFF_Q % 1024 == 0 && OFF_GKB % 1024 == 0, "swizzled tiles are 1024-byte aligned");
 // byte offset of the 16-byte chunk holding channels [c4, c4+4) of row r of the g tile
 __device__ __forceinline__ int g_chunk(int r, int c4) {
     return (c4 >> 5) * (BT * 128) + r * 128 + ((((c4 >> 2) & 7) ^ (r & 7)) << 4);
@@ -428,6 +407,32 @@ __device__ __forceinline__ int g_elem(int r, int c) { return g_chunk(r, c & ~3) 
 // are free of bank conflicts and a group of 4 pairs stays 32 contiguous bytes
 __device__ __forceinline__ int qa_pair(int r, int c) { return r * 512 + ((((c >> 1) ^ ((r & 3) << 2))) << 3); }
 __device__ __forceinline__ int f_pair(int i, int j) { return i * (i - 1) / 2 + j; }
+__device__ __forceinline__ bool f16_ok(float x) { return fabsf(x) < F16_SAFE; }
+// The image leaves in two bulk stores: q_hat (rows 0-63 of A1) and kg as soon
+// as the elementwise step has written them, the rest after the solve.
+__device__ __forceinline__ void store_early(unsigned char *dst, const unsigned char *img) {
+    fence_proxy_async_global();  // after the acquire that found the slot free
+    bulk_s2g(dst + SL_A1, img + SL_A1, 8192);                  // q_hat, channels 0-63
+    bulk_s2g(dst + SL_A1 + 16384, img + SL_A1 + 16384, 8192);  // q_hat, channels 64-127
+    bulk_s2g(dst + SL_KG, img + SL_KG, SL_U - SL_KG);          // kg
+    bulk_commit();
+}
+__device__ __forceinline__ void store_late(unsigned char *dst, const unsigned char *img) {
+    bulk_s2g(dst + SL_A1 + 8192, img + SL_A1 + 8192, 8192);    // w, channels 0-63
+    bulk_s2g(dst + SL_A1 + 24576, img + SL_A1 + 24576, 8192);  // w, channels 64-127
+    bulk_s2g(dst + SL_U, img + SL_U, SLOT_BYTES - SL_U);       // u, e^(G_last), scale*Aqk
+    bulk_commit();
+}
+static_assert(SL_KG == 32768 && SL_U == 49152 && SL_D == 65536 && SL_AQK > SL_D, "slot layout used by the stores");
+
+// slot-image byte offsets of u (token rows of U) and w (rows 64-127 of A1)
+__device__ __forceinline__ int uw_chunk(bool isw, int r, int c8) {
+    return isw ? SL_A1 + tile_chunk(128, 64 + r, c8) : SL_U + tile_chunk(64, r, c8);
+}
+__device__ __forceinline__ int uw_elem(bool isw, int r, int c) { return uw_chunk(isw, r, c & ~7) + ((c & 7) << 1); }
+__device__ __forceinline__ int uw_bk(bool isw, int lane, int k0, int n0) {  // ldmatrix.trans lane address, B [k][n]
+    return isw ? SL_A1 + bk_addr(lane, 128, 64 + k0, n0) : SL_U + bk_addr(lane, 64, k0, n0);
+}
 
 // A task and where its tokens are: t0 = first token of the chunk, nv = its
 // valid rows, h = its head (computed once when the task is drawn).
@@ -473,253 +478,468 @@ __device__ __forceinline__ Task fetch_task(const Params &p, const unsigned char 
     return t;
 }
 
-// 32 bytes of row r of a 128-byte-swizzled tile with `rows` rows per atom
-// column: the 16 16-bit elements at columns c16 .. c16 + 15 (c16 a multiple of
-// 16). Their two 16-byte chunks are adjacent in memory (in swapped order when
-// the row's swizzle is odd), so one 32-byte store writes a whole sector.
-__device__ __forceinline__ void st_row32(unsigned char *tile, int rows, int r, int c16, const uint32_t (&v)[8]) {
-    const int a = (c16 & 63) >> 3, sw = r & 7;
-    unsigned char *q = tile + (c16 >> 6) * rows * 128 + r * 128 + (((a ^ sw) & ~1) << 4);
-    if (sw & 1)
-        asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(q), "r"(v[4]), "r"(v[5]), "r"(v[6]),
-                     "r"(v[7]), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3])
-                     : "memory");
-    else
-        asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(q), "r"(v[0]), "r"(v[1]), "r"(v[2]),
-                     "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
-                     : "memory");
-}
-
-__device__ __forceinline__ unsigned char *slot_of(const Ring &R, const Task &t) {
-    return R.slots + static_cast<size_t>(t.k * RING + t.j % RING) * SLOT_BYTES;
-}
-
-// One task's inputs into shared memory, issued by the `n` threads first ..
-// first + n - 1 once the input tiles are free: 16-byte cp.async copies into
-// the 128-byte-swizzled tile layouts, g (fp32) in a first commit group, q, k, v
-// (bf16) and beta (into buffer bb) in a second, so the prefix sum can start
-// before q, k and v land (every thread waits for its own groups, then the CTA
-// meets at a barrier). Rows past the sequence end are zero-filled (g = 0 keeps
-// row 63 of G at the last valid prefix; k = v = beta = 0 rows are inert in
-// every product).
-__device__ __forceinline__ void issue_loads(const Params &p, unsigned char *smem, const Task &tk, int bb, int first, int n) {
-    const int li = static_cast<int>(threadIdx.x) - first;
+// One task's inputs into shared memory, called by all threads once the
+// buffers are free: 16-byte cp.async copies into the 128-byte-swizzled tile
+// layouts, g (fp32) in a first commit group, q, k, v (bf16) and beta in a
+// second, so the prefix sum can start before q, k and v land. Rows past the
+// sequence end are zero-filled (g = 0 keeps row 63 of G at the last valid
+// prefix; k = v = beta = 0 rows are inert in every product).
+__device__ __forceinline__ void issue_loads(const Params &p, unsigned char *smem, const Task &tk) {
+    const int tid = threadIdx.x;
+    // rows [t0, t0 + nv) of head h; a failed index check zero-fills the task's tiles
+    const bool inb = checked(tk.t0 >= 0 && tk.nv >= 0 && tk.nv <= BT && static_cast<int64_t>(tk.t0) + tk.nv <= p.Ttok &&
+                                 tk.h >= 0 && tk.h < p.H,
+                             p.status);
+    const int t0 = inb ? tk.t0 : 0, nv = inb ? tk.nv : 0, h = inb ? tk.h : 0;
     const size_t rs = static_cast<size_t>(p.H) * DK;  // token stride, elements
-    const size_t hb = static_cast<size_t>(tk.h) * DK;
-    for (int idx = li; idx < BT * 32; idx += n) {  // g: 64 rows x 32 chunks of 4 channels
-        const int r = idx >> 5, c4 = (idx & 31) << 2;
-        const bool ok = r < tk.nv;
-        cp_async16(smem + OFF_G + g_chunk(r, c4), p.g + static_cast<size_t>(tk.t0 + (ok ? r : 0)) * rs + hb + c4,
+    const size_t hb = static_cast<size_t>(h) * DK;
+    KDA_TRACE_EV(p, 30, 0);
+#pragma unroll
+    for (int it = 0; it < BT * 32 / NCOMP; ++it) {  // g: 64 rows x 32 chunks of 4 channels
+        const int idx = tid + it * NCOMP, r = idx >> 5, c4 = (idx & 31) << 2;
+        const bool ok = r < nv;
+        cp_async16(smem + OFF_GKB + g_chunk(r, c4), p.g + static_cast<size_t>(t0 + (ok ? r : 0)) * rs + hb + c4,
                    ok ? 16 : 0);
     }
-    if (p.raw && li < 33) {  // the gate activation's per-head parameters (zeros when not given)
-        if (li < 32)
-            cp_async16(smem + OFF_GPAR + 16 * li, p.dt_bias ? p.dt_bias + hb + 4 * li : p.g, p.dt_bias ? 16 : 0);
+    if (p.raw && tid < 33) {  // the gate activation's per-head parameters (zeros when not given)
+        if (tid < 32)
+            cp_async16(smem + OFF_GPAR + 16 * tid, p.dt_bias ? p.dt_bias + hb + 4 * tid : p.g, p.dt_bias ? 16 : 0);
         else
-            cp_async4(smem + OFF_GPAR + 512, p.A_log ? p.A_log + tk.h : p.g, p.A_log ? 4 : 0);
+            cp_async4(smem + OFF_GPAR + 512, p.A_log ? p.A_log + h : p.g, p.A_log ? 4 : 0);
     }
     cp_async_commit();
-    for (int idx = li; idx < BT * 16; idx += n) {  // q, k, v: 64 rows x 16 chunks of 8 channels
-        const int r = idx >> 4, c8 = (idx & 15) << 3;
-        const bool ok = r < tk.nv;
-        const size_t off = static_cast<size_t>(tk.t0 + (ok ? r : 0)) * rs + hb + c8;
+#pragma unroll
+    for (int it = 0; it < BT * 16 / NCOMP; ++it) {  // q, k, v: 64 rows x 16 chunks of 8 channels
+        const int idx = tid + it * NCOMP, r = idx >> 4, c8 = (idx & 15) << 3;
+        const bool ok = r < nv;
+        const size_t off = static_cast<size_t>(t0 + (ok ? r : 0)) * rs + hb + c8;
         const int d = tile_chunk(64, r, c8);
         cp_async16(smem + OFF_Q + d, p.q + off, ok ? 16 : 0);
         cp_async16(smem + OFF_K + d, p.k + off, ok ? 16 : 0);
         cp_async16(smem + OFF_V + d, p.v + off, ok ? 16 : 0);
     }
-    if (li >= n - BT) {  // the last 64 threads: beta
-        const int r = li - (n - BT);
-        const bool ok = r < tk.nv;
-        cp_async4(smem + OFF_BETA + 256 * bb + 4 * r, p.beta + static_cast<size_t>(tk.t0 + (ok ? r : 0)) * p.H + tk.h,
-                  ok ? 4 : 0);
+    if (tid >= NCOMP - BT) {  // warps 14 and 15
+        const int r = tid - (NCOMP - BT);
+        const bool ok = r < nv;
+        cp_async4(smem + OFF_BETA + 4 * r, p.beta + static_cast<size_t>(t0 + (ok ? r : 0)) * p.H + h, ok ? 4 : 0);
     }
     cp_async_commit();
 }
 
-// The previous task's WY product X^T = [u | w]^T, read out of tensor memory
-// into the previous task's slot: u^T rows into U, w^T rows into atom column 1
-// of B1 (this thread: channel `chn`, tokens 16 b .. 16 b + 15 for b in [b0, b1)).
-__device__ __forceinline__ void read_out_x(uint32_t tl, unsigned char *pd, int chn, int b0, int b1, float &vmax) {
-    for (int b = b0; b < b1; ++b) {
-        uint32_t xu[16], xw[16];
-        tmem_ld16(tl + TM_XU + 16 * b, xu);
-        tmem_ld16(tl + TM_XW + 16 * b, xw);
-        tmem_wait_ld();
-        uint32_t u2[8], w2[8];
-        float vm = vmax;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const float a0 = __uint_as_float(xu[2 * e]), a1 = __uint_as_float(xu[2 * e + 1]);
-            const float c0 = __uint_as_float(xw[2 * e]), c1 = __uint_as_float(xw[2 * e + 1]);
-            vm = max_abs_nan(max_abs_nan(vm, a0), a1);
-            vm = max_abs_nan(max_abs_nan(vm, c0), c1);
-            u2[e] = pack_f16(a0, a1);
-            w2[e] = pack_f16(c0, c1);
-        }
-        vmax = vm;
-        st_row32(pd + SL_U, 128, chn, 16 * b, u2);
-        st_row32(pd + SL_B1, 128, chn, 64 + 16 * b, w2);
-    }
-}
+// One (chain, chunk) task: steps 1-4 into the slot image, then the bulk store
+// of the image into the task's slot. Its inputs were loaded by issue_loads.
+// `nxt` is the next task (drawn one task earlier); its input copies start
+// right after the strips.
+// During the strips, REL_TID completes and publishes the previous task's slot
+// (`pending` = its ready-flag index or -1, `pending_val` the value) while
+// SYNC_TID draws the task after `nxt` into `nxt2` and waits for this task's
+// slot to be free. The publication waits only for this CTA's own bulk store,
+// never for a consumer, so a producer never waits on a consumer while its
+// finished chunk stays unpublished (and tasks drawn but not started wait on
+// nothing: the lowest-numbered unpublished task can always proceed).
+// Returns false when the slot wait gave up (timeout or abort).
+__device__ __forceinline__ bool run_task(const Params &p, const Ring &Rg, unsigned char *smem, const Task &cur,
+                                         const int32_t *cu_s, int jmax, const Task &nxt, Task &nxt2, Cursor &cs, int &pending,
+                                         int pending_val, bool &gate_bad, bool &range_bad) {
+    unsigned char *img = smem + OFF_IMG;
+    unsigned char *sQ = smem + OFF_Q, *sK = smem + OFF_K, *sV = smem + OFF_V;
+    unsigned char *sGb = smem + OFF_GKB;  // G, swizzled (g_chunk / g_elem)
+    float *sKB = reinterpret_cast<float *>(smem + OFF_GKB);
+    __half *sL = reinterpret_cast<__half *>(smem + OFF_L);
+    float *sLD = reinterpret_cast<float *>(smem + OFF_LD);
+    __half *sT = reinterpret_cast<__half *>(smem + OFF_T);
+    float *sTab = reinterpret_cast<float *>(smem + OFF_TAB);
+    float *sBeta = reinterpret_cast<float *>(smem + OFF_BETA);
+    int *misc = reinterpret_cast<int *>(smem + OFF_MISC);
 
-// a slot's ready flag, released once the slot's contents have been written
-// (all of them ordered before this thread by a preceding barrier)
-__device__ __forceinline__ void publish(const Params &p, const Ring &R, const Task &t) {
-    fence_acq_rel_gpu();
-    if (!(p.debug & KDA_DEBUG_WITHHOLD_READY)) st_release(&R.ready[t.k * RING + t.j % RING], t.j + 1);
-}
-// whether task t's slot is free (its consumer has copied out the chunk that
-// used it RING chunks earlier), polling at most `polls` times
-__device__ __forceinline__ bool slot_free(const Ring &R, const Task &t, long long polls) {
-    if (t.j < RING) return true;
-    const int *f = &R.freed[t.k * RING + t.j % RING];
-    for (long long it = 0; it < polls; ++it) {
-        if (ld_acquire(f) >= t.j - RING + 1) return true;
-        __nanosleep(64);
-    }
-    return false;
-}
-
-// Step 2b for one group of strip tiles on one warp: row blocks R0 and R0 + 1
-// against column blocks C0 .. C0 + NC - 1 (the tiles (i, j) with j <= i among
-// them), so that each 16-channel step loads the A fragments of a row block and
-// the B values of a column block once for all the group's tiles. Aqk on tf32
-// (m16n8k8), Akk on bf16 (m16n8k16). Within each 16-channel step the tf32 k
-// slots are permuted (slot q <-> channel 2q, slot q+4 <-> channel 2q+1, for each
-// half) so that one 8-byte load of a k e^(G_m - G) row feeds both the tf32 and
-// the bf16 B fragments. Tile (i, j) needs k_s e^(G_{m_i} - G_s) for s in
-// sub-block j: the stored k e^(G_{m_j} - G) times e^(G_{m_i} - G_{m_j}) (<= 1).
-// Writes scale*Aqk into the slot and L = diag(beta) tril(Akk, -1) (and its
-// diagonal blocks in fp32) into shared memory.
-template <int R0, int C0, int NC>
-__device__ __forceinline__ void strip_group(const unsigned char *smem, unsigned char *dst, const float *sBeta, float scale,
-                                            int lane) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int gq = lane >> 2, qd = lane & 3;
-    const float *sKB = reinterpret_cast<const float *>(smem + OFF_KB);
-    const float *sF = reinterpret_cast<const float *>(smem + OFF_F);
-    __half *sL = reinterpret_cast<__half *>(const_cast<unsigned char *>(smem) + OFF_L);
-    float *sLD = reinterpret_cast<float *>(const_cast<unsigned char *>(smem) + OFF_LD);
-    float aq[2][NC][2][4], ak[2][NC][2][4];
+    const float scale = p.scale;
+    // ---- step 1: inclusive prefix sum of g (base 2) per key channel, four
+    // 16-row quarters per channel on all 512 threads, then the per-channel tables
+    {
+        const int chn = tid & 127, rq = tid >> 7;
+        float x[16];
 #pragma unroll
-    for (int ri = 0; ri < 2; ++ri)
+        for (int q = 0; q < 16; ++q) x[q] = *reinterpret_cast<const float *>(sGb + g_elem(16 * rq + q, chn));
+        if (p.raw) {  // g = lower_bound * sigmoid(e^A_log (g_raw + dt_bias)); rows past the sequence end stay 0
+            const float *gp = reinterpret_cast<const float *>(smem + OFF_GPAR);
+            const float a = __expf(gp[128]), db = gp[chn];
 #pragma unroll
-        for (int cj = 0; cj < NC; ++cj)
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) aq[ri][cj][nt][e] = ak[ri][cj][nt][e] = 0.f;
-#pragma unroll 2
-    for (int kk = 0; kk < 8; ++kk) {
-        const int c0 = 16 * kk + 2 * qd;
-        uint32_t fa0[2][4], fa1[2][4], fk[2][4];
-#pragma unroll
-        for (int ri = 0; ri < 2; ++ri) {
-            const int i = R0 + ri;
-            const unsigned char *sQA = smem + OFF_QA;
-            const uint2 u00 = *reinterpret_cast<const uint2 *>(sQA + qa_pair(16 * i + gq, c0));
-            const uint2 u10 = *reinterpret_cast<const uint2 *>(sQA + qa_pair(16 * i + gq + 8, c0));
-            const uint2 u01 = *reinterpret_cast<const uint2 *>(sQA + qa_pair(16 * i + gq, c0 + 8));
-            const uint2 u11 = *reinterpret_cast<const uint2 *>(sQA + qa_pair(16 * i + gq + 8, c0 + 8));
-            fa0[ri][0] = u00.x; fa0[ri][1] = u10.x; fa0[ri][2] = u00.y; fa0[ri][3] = u10.y;
-            fa1[ri][0] = u01.x; fa1[ri][1] = u11.x; fa1[ri][2] = u01.y; fa1[ri][3] = u11.y;
-            ldsm_x4(fk[ri], smem + OFF_KA + a_addr(lane, 64, 16 * i, 16 * kk));
+            for (int q = 0; q < 16; ++q)
+                x[q] = (16 * rq + q < cur.nv) ? __fdividef(p.lb, 1.f + __expf(-a * (x[q] + db))) : 0.f;
         }
-        float2 x0[NC][2], x1[NC][2];
+        float acc = 0.f;
+        bool gb = false;
 #pragma unroll
-        for (int cj = 0; cj < NC; ++cj)
+        for (int q = 0; q < 16; ++q) {
+            gb |= !(x[q] >= p.lb && x[q] <= 0.f);
+            acc += x[q] * LOG2E;
+            x[q] = acc;
+        }
+        gate_bad |= gb;
+        sTab[TEM + rq * 128 + chn] = acc;  // quarter totals (the EM rows are rebuilt below)
+        sync_compute();
+        float cy = 0.f;
+        for (int q = 0; q < rq; ++q) cy += sTab[TEM + q * 128 + chn];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) *reinterpret_cast<float *>(sGb + g_elem(16 * rq + q, chn)) = x[q] + cy;
+    }
+    sync_compute();
+    if (tid < DK) {  // rows >= nv carry g = 0, so row 63 holds the last valid prefix
+        const int chn = tid;
+        float gm[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) gm[i] = *reinterpret_cast<const float *>(sGb + g_elem(16 * i + 7, chn));
+        const float gl = *reinterpret_cast<const float *>(sGb + g_elem(63, chn));
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            sTab[TGM + i * 128 + chn] = gm[i];
+            sTab[TEM + i * 128 + chn] = ex2(gm[i]);
+            sTab[TEL + i * 128 + chn] = ex2(gl - gm[i]);
+        }
+        sTab[TGL + chn] = gl;
+        sTab[TD + chn] = ex2(gl);
+#pragma unroll
+        for (int i = 1; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < i; ++j) sTab[TF + f_pair(i, j) * 128 + chn] = ex2(gm[i] - gm[j]);
+    }
+    if (tid == REL_TID) bulk_wait_read();  // the previous image has been read out and may be rewritten
+    cp_async_wait_all();  // q, k, v and beta
+    sync_compute();
+    if (p.raw) {  // beta = sigmoid(beta_raw); rows past the sequence end stay 0
+        if (tid < BT) sBeta[tid] = tid < cur.nv ? __fdividef(1.f, 1.f + __expf(-sBeta[tid])) : 0.f;
+        sync_compute();
+    }
+    KDA_TRACE_EV(p, 21, 0);
+
+    // ---- steps 2a/4a: elementwise operands; q_hat, kg, beta*v and
+    // beta*k*e^G go straight into the slot image
+    {
+        // thread: channels c8..c8+7 of rows r0 and r0 + 8, both in sub-block i
+        const int ew_i = tid >> 7, ew_c8 = (tid & 15) << 3, ew_r0 = 16 * ew_i + ((tid >> 4) & 7);
+        float Gv[2][8];
+        uint4 qv[2], kv[2], vv[2];
+#pragma unroll
+        for (int it = 0; it < 2; ++it) {
+            const int r = ew_r0 + 8 * it, c8 = ew_c8;
+            const float4 a = *reinterpret_cast<const float4 *>(sGb + g_chunk(r, c8));
+            const float4 b = *reinterpret_cast<const float4 *>(sGb + g_chunk(r, c8 + 4));
+            Gv[it][0] = a.x; Gv[it][1] = a.y; Gv[it][2] = a.z; Gv[it][3] = a.w;
+            Gv[it][4] = b.x; Gv[it][5] = b.y; Gv[it][6] = b.z; Gv[it][7] = b.w;
+            const int tc = tile_chunk(64, r, c8);
+            qv[it] = *reinterpret_cast<const uint4 *>(sQ + tc);
+            kv[it] = *reinterpret_cast<const uint4 *>(sK + tc);
+            vv[it] = *reinterpret_cast<const uint4 *>(sV + tc);
+        }
+        sync_compute();  // G and q are read: kb and q*a overwrite them below
+        float GM[8], EM[8], EL[8];
+        {
+            const int i = ew_i, c8 = ew_c8;
+            const float4 a0 = *reinterpret_cast<const float4 *>(sTab + TGM + i * 128 + c8);
+            const float4 a1 = *reinterpret_cast<const float4 *>(sTab + TGM + i * 128 + c8 + 4);
+            const float4 b0 = *reinterpret_cast<const float4 *>(sTab + TEM + i * 128 + c8);
+            const float4 b1 = *reinterpret_cast<const float4 *>(sTab + TEM + i * 128 + c8 + 4);
+            const float4 d0 = *reinterpret_cast<const float4 *>(sTab + TEL + i * 128 + c8);
+            const float4 d1 = *reinterpret_cast<const float4 *>(sTab + TEL + i * 128 + c8 + 4);
+            GM[0] = a0.x; GM[1] = a0.y; GM[2] = a0.z; GM[3] = a0.w; GM[4] = a1.x; GM[5] = a1.y; GM[6] = a1.z; GM[7] = a1.w;
+            EM[0] = b0.x; EM[1] = b0.y; EM[2] = b0.z; EM[3] = b0.w; EM[4] = b1.x; EM[5] = b1.y; EM[6] = b1.z; EM[7] = b1.w;
+            EL[0] = d0.x; EL[1] = d0.y; EL[2] = d0.z; EL[3] = d0.w; EL[4] = d1.x; EL[5] = d1.y; EL[6] = d1.z; EL[7] = d1.w;
+        }
+#pragma unroll
+        for (int it = 0; it < 2; ++it) {
+            const int r = ew_r0 + 8 * it, c8 = ew_c8;
+            const float bt = sBeta[r];
+            const int tc = tile_chunk(64, r, c8);
+            const uint32_t *qw = reinterpret_cast<const uint32_t *>(&qv[it]);
+            const uint32_t *kw = reinterpret_cast<const uint32_t *>(&kv[it]);
+            const uint32_t *vw = reinterpret_cast<const uint32_t *>(&vv[it]);
+            uint32_t oQa[8], oKa[4], oBv[4], oBk[4], oQs[4], oKg[4];
+            float kb[8];
+#pragma unroll
+            for (int q2 = 0; q2 < 4; ++q2) {
+                const float2 qf = unpack_bf16(qw[q2]), kf = unpack_bf16(kw[q2]), vf = unpack_bf16(vw[q2]);
+                float res[2][6];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int ce = 2 * q2 + e;
+                    const float qq = e ? qf.y : qf.x, kk = e ? kf.y : kf.x, vv2 = e ? vf.y : vf.x;
+                    const float x = Gv[it][ce] - GM[ce];
+                    const float a = ex2(x), b = ex2(-x);
+                    const float eG = a * EM[ce];
+                    res[e][0] = qq * a;            // q e^(G - G_m)
+                    res[e][1] = kk * a;            // k e^(G - G_m)
+                    res[e][2] = bt * vv2;          // beta v
+                    res[e][3] = bt * kk * eG;      // beta k e^G
+                    res[e][4] = scale * qq * eG;   // scale q e^G
+                    res[e][5] = kk * b * EL[ce];   // k e^(G_last - G)
+                    kb[ce] = kk * b;               // k e^(G_m - G)
+                }
+                oQa[2 * q2] = tf32_rna(res[0][0]);
+                oQa[2 * q2 + 1] = tf32_rna(res[1][0]);
+                oKa[q2] = pack_bf16(res[0][1], res[1][1]);
+                range_bad |= !(f16_ok(res[0][2]) && f16_ok(res[1][2]) && f16_ok(res[0][3]) && f16_ok(res[1][3]) &&
+                               f16_ok(res[0][4]) && f16_ok(res[1][4]) && f16_ok(res[0][5]) && f16_ok(res[1][5]));
+                oBv[q2] = pack_f16(res[0][2], res[1][2]);
+                oBk[q2] = pack_f16(res[0][3], res[1][3]);
+                oQs[q2] = pack_f16(res[0][4], res[1][4]);
+                oKg[q2] = pack_f16(res[0][5], res[1][5]);
+            }
+            *reinterpret_cast<uint4 *>(sQ + qa_pair(r, c8)) = make_uint4(oQa[0], oQa[1], oQa[2], oQa[3]);
+            *reinterpret_cast<uint4 *>(sQ + qa_pair(r, c8) + 16) = make_uint4(oQa[4], oQa[5], oQa[6], oQa[7]);
+            *reinterpret_cast<uint4 *>(sK + tc) = *reinterpret_cast<uint4 *>(oKa);
+            *reinterpret_cast<float4 *>(sKB + r * RSF + c8) = make_float4(kb[0], kb[1], kb[2], kb[3]);
+            *reinterpret_cast<float4 *>(sKB + r * RSF + c8 + 4) = make_float4(kb[4], kb[5], kb[6], kb[7]);
+            *reinterpret_cast<uint4 *>(img + uw_chunk(false, r, c8)) = *reinterpret_cast<uint4 *>(oBv);
+            *reinterpret_cast<uint4 *>(img + uw_chunk(true, r, c8)) = *reinterpret_cast<uint4 *>(oBk);
+            *reinterpret_cast<uint4 *>(img + SL_A1 + tile_chunk(128, r, c8)) = *reinterpret_cast<uint4 *>(oQs);
+            *reinterpret_cast<uint4 *>(img + SL_KG + tile_chunk(64, r, c8)) = *reinterpret_cast<uint4 *>(oKg);
+        }
+        if (tid < 32)
+            *reinterpret_cast<float4 *>(img + SL_D + 16 * tid) = *reinterpret_cast<const float4 *>(sTab + TD + 4 * tid);
+    }
+    // the image parts just written are read by the early bulk store, and the
+    // input tiles just written (q*a, k*a, kb) are rewritten by the next tensor
+    // copies: order these generic writes before both
+    fence_proxy_async_shared();
+    sync_compute();
+    KDA_TRACE_EV(p, 22, 0);
+
+    // ---- ring work, on warps 12 and 13 (no strip pair, no diagonal block).
+    // REL_TID: publish the previous slot, then wait for this task's slot and
+    // send the part of the image that is final already. SYNC_TID: draw.
+    const bool slot_inb = checked(cur.k >= 0 && cur.k < p.C && cur.j >= 0, p.status);
+    unsigned char *dst = Rg.slots + static_cast<size_t>(slot_inb ? cur.k * RING + cur.j % RING : 0) * SLOT_BYTES;
+    if (tid == REL_TID) {
+        if (pending >= 0) {
+            bulk_wait_all();
+            fence_proxy_async_global();
+            if (!(p.debug & KDA_DEBUG_WITHHOLD_READY)) st_release(&Rg.ready[pending], pending_val);
+            pending = -1;
+        }
+        KDA_TRACE_ANY(p, 31, 0);
+        const int s = cur.j % RING;
+        const bool free_ok =
+            slot_inb && ((cur.j < RING) || wait_flag_geq(Rg, &Rg.freed[cur.k * RING + s], cur.j - RING + 1, p.status));
+        misc[20] = free_ok ? 1 : 0;
+        if (free_ok) store_early(dst, img);
+        KDA_TRACE_ANY(p, 33, 0);
+    }
+    if (tid == SYNC_TID) {
+        const Task t = fetch_task(p, smem, cu_s, jmax, cs);
+        put_task(misc + 2, t);
+        KDA_TRACE_ANY(p, 35, 0);
+    }
+    // ---- step 2b: Aqk (tf32) and Akk (bf16) on the 10
+    // lower 16x16 tiles, one tile per warp. Tile (i,j) needs k_s e^(G_{m_i} - G_s)
+    // for s in sub-block j: the stored k e^(G_{m_j} - G) times e^(G_{m_i} - G_{m_j}) (<= 1).
+    static_assert(NWARPS == 16, "warps 0-9 strips, 10, 11, 14, 15 diagonal inverses, 12-13 ring work");
+    // Warp w runs on sub-partition w % 4, so warps 0-9 leave partitions 0 and 1
+    // with three tiles and 2 and 3 with two: the diagonal tiles (pairs 0, 2, 5,
+    // 9), whose L_ii feed the inverses, go to warps 2, 3, 6, 7 on the lighter ones.
+    if (warp < 10) {
+        const int pair = (0x8795642031ull >> (4 * warp)) & 15;  // warp -> pair: 1 3 0 2 4 6 5 9 7 8
+        int i = 0;
+        while ((i + 1) * (i + 2) / 2 <= pair) ++i;
+        const int j = pair - i * (i + 1) / 2;
+        const float *kbrow0 = sKB + (16 * j + gq) * RSF;      // column s = 16j + gq
+        const float *kbrow1 = sKB + (16 * j + 8 + gq) * RSF;  // column s = 16j + 8 + gq
+        const float *fr = sTab + TF + (i > j ? f_pair(i, j) : 0) * 128;
+        float aq[2][4] = {}, ak[2][4] = {};
+        // Aqk on tf32 (m16n8k8), Akk on bf16 (m16n8k16). Within each 16-channel
+        // step the tf32 k slots are permuted (slot q <-> channel 2q, slot q+4 <->
+        // channel 2q+1, for each half) so that one 8-byte load of the scaled
+        // k row feeds both the tf32 and the bf16 B fragments.
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            const int c0 = 16 * kk + 2 * qd;
+            uint32_t fa0[4], fa1[4], fk[4];
+            {
+                const uint2 u00 = *reinterpret_cast<const uint2 *>(sQ + qa_pair(16 * i + gq, c0));
+                const uint2 u10 = *reinterpret_cast<const uint2 *>(sQ + qa_pair(16 * i + gq + 8, c0));
+                const uint2 u01 = *reinterpret_cast<const uint2 *>(sQ + qa_pair(16 * i + gq, c0 + 8));
+                const uint2 u11 = *reinterpret_cast<const uint2 *>(sQ + qa_pair(16 * i + gq + 8, c0 + 8));
+                fa0[0] = u00.x; fa0[1] = u10.x; fa0[2] = u00.y; fa0[3] = u10.y;
+                fa1[0] = u01.x; fa1[1] = u11.x; fa1[2] = u01.y; fa1[3] = u11.y;
+            }
+            ldsm_x4(fk, sK + a_addr(lane, 64, 16 * i, 16 * kk));
+            float2 f0 = make_float2(1.f, 1.f), f1 = make_float2(1.f, 1.f);
+            if (i > j) {
+                f0 = *reinterpret_cast<const float2 *>(fr + c0);
+                f1 = *reinterpret_cast<const float2 *>(fr + c0 + 8);
+            }
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
-                const float *row = sKB + (16 * (C0 + cj) + 8 * nt + gq) * RSF;
-                x0[cj][nt] = *reinterpret_cast<const float2 *>(row + c0);
-                x1[cj][nt] = *reinterpret_cast<const float2 *>(row + c0 + 8);
+                const float *row = nt ? kbrow1 : kbrow0;
+                const float2 x0 = *reinterpret_cast<const float2 *>(row + c0);
+                const float2 x1 = *reinterpret_cast<const float2 *>(row + c0 + 8);
+                const float b00 = x0.x * f0.x, b01 = x0.y * f0.y, b10 = x1.x * f1.x, b11 = x1.y * f1.y;
+                mma1688_tf32(aq[nt], fa0, tf32_rna(b00), tf32_rna(b01));
+                mma1688_tf32(aq[nt], fa1, tf32_rna(b10), tf32_rna(b11));
+                mma16816(ak[nt], fk, pack_bf16(b00, b01), pack_bf16(b10, b11));
             }
+        }
 #pragma unroll
-        for (int ri = 0; ri < 2; ++ri)
+        for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-            for (int cj = 0; cj < NC; ++cj) {
-                const int i = R0 + ri, j = C0 + cj;
-                if (j > i) continue;
-                float2 f0 = make_float2(1.f, 1.f), f1 = make_float2(1.f, 1.f);
-                if (i > j) {
-                    const float *fr = sF + f_pair(i, j) * 128;
-                    f0 = *reinterpret_cast<const float2 *>(fr + c0);
-                    f1 = *reinterpret_cast<const float2 *>(fr + c0 + 8);
+            for (int hf = 0; hf < 2; ++hf) {
+                const int tl = gq + 8 * hf, sl = 8 * nt + 2 * qd;
+                const int t = 16 * i + tl, s = 16 * j + sl;
+                const float bt = sBeta[t];
+                float vq[2], vk[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const bool incl = (i > j) || (sl + e <= tl);
+                    const bool strict = (i > j) || (sl + e < tl);
+                    vq[e] = incl ? scale * aq[nt][2 * hf + e] : 0.f;
+                    vk[e] = strict ? bt * ak[nt][2 * hf + e] : 0.f;
+                    if (i == j) sLD[(i * 16 + tl) * 17 + sl + e] = vk[e];
+                    range_bad |= !(f16_ok(vq[e]) && f16_ok(vk[e]));
                 }
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    const float b00 = x0[cj][nt].x * f0.x, b01 = x0[cj][nt].y * f0.y;
-                    const float b10 = x1[cj][nt].x * f1.x, b11 = x1[cj][nt].y * f1.y;
-                    mma1688_tf32(aq[ri][cj][nt], fa0[ri], tf32_rna(b00), tf32_rna(b01));
-                    mma1688_tf32(aq[ri][cj][nt], fa1[ri], tf32_rna(b10), tf32_rna(b11));
-                    mma16816(ak[ri][cj][nt], fk[ri], pack_bf16(b00, b01), pack_bf16(b10, b11));
-                }
+                *reinterpret_cast<uint32_t *>(img + SL_AQK + tile_elem(64, t, s)) = pack_f16(vq[0], vq[1]);
+                *reinterpret_cast<uint32_t *>(sL + t * RSA + s) = pack_f16(vk[0], vk[1]);
             }
+        if (i == j) {  // L_ii is in place: hand it to the inverse warp of block i
+            __syncwarp();
+            named_bar_arrive(2 + i, 64);
+        }
+        if (lane == 0) KDA_TRACE_ANY(p, 40 + warp, 0);
     }
+    // ---- step 3a, on warps 10, 11, 14, 15 (blocks 0-3) while the strips run:
+    // T_ii = (I + L_ii)^-1 by fp32 forward substitution, once the warp with
+    // tile (i, i) has written L_ii
+    if (warp == 10 || warp == 11 || warp == 14 || warp == 15) {
+        const int i = (warp & 1) | ((warp & 4) >> 1);
+        named_bar_sync(2 + i, 64);
+        if (lane < 16) {
+            const int jc = lane;
+            const float *Ld = sLD + i * 16 * 17;
+            float x[16];
 #pragma unroll
-    for (int ri = 0; ri < 2; ++ri)
+            for (int r = 0; r < 16; ++r) {
+                float s = (r == jc) ? 1.f : 0.f;
 #pragma unroll
-        for (int cj = 0; cj < NC; ++cj) {
-            const int i = R0 + ri, j = C0 + cj;
-            if (j > i) continue;
+                for (int cc = 0; cc < r; ++cc) s -= Ld[r * 17 + cc] * x[cc];
+                x[r] = s;
+            }
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+                range_bad |= !f16_ok(x[r]);
+                sT[(16 * i + r) * RSA + 16 * i + jc] = __float2half_rn(x[r]);
+            }
+        }
+        if (lane == 0) KDA_TRACE_ANY(p, 50 + i, 0);
+    }
+    sync_compute();  // the strips only read the input tiles: their values are in registers by now
+    nxt2 = get_task(misc + 2);
+    const bool slot_ok = misc[20] != 0;
+    // q, k, v, q*a lo, kb and beta are free: stream in the next task
+    if (nxt.valid) issue_loads(p, smem, nxt);
+    if (!slot_ok) return false;
+    KDA_TRACE_EV(p, 23, 0);
+
+    // ---- steps 3b and 4, interleaved. Block row i of X = [u | w] =
+    // T [beta v | beta k e^G] needs block rows 0..i of T = (I + L)^-1 only, so
+    // while all warps compute X_i, warps 0 .. 2-i build block diagonal i+1 of T:
+    // T_ij = -T_ii * sum_{k=j}^{i-1} L_ik T_kj. X is written in place in the
+    // slot image (u in U, w in rows 64-127 of A1); warp w owns 16 columns and
+    // holds all four row blocks of them in registers before it writes any.
+    {
+        const bool isw = warp >= 8;
+        const int col0 = 16 * (warp & 7);
+        uint32_t rb[4][4];
+#pragma unroll
+        for (int kb = 0; kb < 4; ++kb) ldsm_x4_t(rb[kb], img + uw_bk(isw, lane, 16 * kb, col0));
+#pragma unroll
+        for (int xi = 0; xi < 4; ++xi) {
+            const int d = xi + 1;
+            if (d < 4 && warp < 4 - d) {
+                const int j = warp, i = warp + d;
+                float m[2][4] = {};
+                for (int kb = j; kb < i; ++kb) {
+                    uint32_t fa[4], fb[4];
+                    ldsm_x4(fa, sL + (16 * i + (lane & 15)) * RSA + 16 * kb + ((lane >> 4) << 3));
+                    ldsm_x4_t(fb, sT + bk_off(lane, 16 * kb, 16 * j, RSA));
+                    mma16816_f16(m[0], fa, fb[0], fb[1]);
+                    mma16816_f16(m[1], fa, fb[2], fb[3]);
+                }
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {
+                        range_bad |= !(f16_ok(m[nt][2 * hf]) && f16_ok(m[nt][2 * hf + 1]));
+                        *reinterpret_cast<uint32_t *>(sT + (16 * i + gq + 8 * hf) * RSA + 16 * j + 8 * nt + 2 * qd) =
+                            pack_f16(m[nt][2 * hf], m[nt][2 * hf + 1]);
+                    }
+                __syncwarp();
+                float t[2][4] = {};
+                {
+                    uint32_t fa[4], fb[4];
+                    ldsm_x4(fa, sT + (16 * i + (lane & 15)) * RSA + 16 * i + ((lane >> 4) << 3));
+                    ldsm_x4_t(fb, sT + bk_off(lane, 16 * i, 16 * j, RSA));
+                    mma16816_f16(t[0], fa, fb[0], fb[1]);
+                    mma16816_f16(t[1], fa, fb[2], fb[3]);
+                }
+                __syncwarp();
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {
+                        range_bad |= !(f16_ok(t[nt][2 * hf]) && f16_ok(t[nt][2 * hf + 1]));
+                        *reinterpret_cast<uint32_t *>(sT + (16 * i + gq + 8 * hf) * RSA + 16 * j + 8 * nt + 2 * qd) =
+                            pack_f16(-t[nt][2 * hf], -t[nt][2 * hf + 1]);
+                    }
+            }
+            float acc[2][4] = {};
+#pragma unroll
+            for (int kb = 0; kb <= xi; ++kb) {
+                uint32_t fa[4];
+                ldsm_x4(fa, sT + (16 * xi + (lane & 15)) * RSA + 16 * kb + ((lane >> 4) << 3));
+                mma16816_f16(acc[0], fa, rb[kb][0], rb[kb][1]);
+                mma16816_f16(acc[1], fa, rb[kb][2], rb[kb][3]);
+            }
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
-                    const int tl16 = gq + 8 * hf, sl = 8 * nt + 2 * qd;
-                    const int t = 16 * i + tl16, sc = 16 * j + sl;
-                    const float btt = sBeta[t];
-                    float vq[2], vk[2];
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const bool incl = (i > j) || (sl + e <= tl16);
-                        const bool strict = (i > j) || (sl + e < tl16);
-                        vq[e] = incl ? scale * aq[ri][cj][nt][2 * hf + e] : 0.f;
-                        vk[e] = strict ? btt * ak[ri][cj][nt][2 * hf + e] : 0.f;
-                        if (i == j) sLD[(i * 16 + tl16) * 17 + sl + e] = vk[e];
-                    }
-                    *reinterpret_cast<uint32_t *>(dst + SL_B23 + tile_elem(192, 128 + t, sc)) = pack_f16(vq[0], vq[1]);
-                    *reinterpret_cast<uint32_t *>(sL + t * RSA + sc) = pack_f16(vk[0], vk[1]);
+                    const int rr = 16 * xi + gq + 8 * hf, cc = col0 + 8 * nt + 2 * qd;
+                    range_bad |= !(f16_ok(acc[nt][2 * hf]) && f16_ok(acc[nt][2 * hf + 1]));
+                    *reinterpret_cast<uint32_t *>(img + uw_elem(isw, rr, cc)) = pack_f16(acc[nt][2 * hf], acc[nt][2 * hf + 1]);
                 }
+            if (xi < 3) sync_compute();  // block diagonal d of T is complete
         }
+    }
+    KDA_TRACE_EV(p, 24, 0);
+    fence_proxy_async_shared();  // this thread's image writes, before the bulk store reads them
+    sync_compute();
+    KDA_TRACE_EV(p, 25, 0);
+
+    // ---- hand-off: the rest of the image (published by REL_TID during the
+    // next task's strips, or after the last task)
+    if (tid == REL_TID) store_late(dst, img);
+    return true;
 }
 
 __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int pid) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int quad = warp & 3, blk = warp >> 2;  // channel group (tensor-memory lane quarter), sub-block
-    const int chn = 32 * quad + lane;            // this thread's key channel
-    const int gq = lane >> 2, qd = lane & 3;
-    const float scale = p.scale;
+    const int tid = threadIdx.x;
     Ring R = ring_of(p);
     int *misc = reinterpret_cast<int *>(smem + OFF_MISC);
-    uint64_t *bar_x = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + OFF_BAR + 8);
-    float *sTot = reinterpret_cast<float *>(smem + OFF_TOT);
-    float *sGm = reinterpret_cast<float *>(smem + OFF_GM);
-    float *sF = reinterpret_cast<float *>(smem + OFF_F);
-    float *sKB = reinterpret_cast<float *>(smem + OFF_KB);
-    __half *sL = reinterpret_cast<__half *>(smem + OFF_L);
-    float *sLD = reinterpret_cast<float *>(smem + OFF_LD);
-    unsigned char *sT = smem + OFF_T;
     const int32_t *cu_s = sched_cu(p, smem);  // sequence bounds (in shared memory when small enough)
-
-    // the upper blocks of T are never written: zero the tile once
-    for (int i = tid; i < 8192 / 16; i += NCOMP) reinterpret_cast<uint4 *>(sT)[i] = make_uint4(0, 0, 0, 0);
-    if (tid == 0) {
-        misc[1] = 0;
-        mbar_init(bar_x, 1);
-        mbar_fence_init();
-    }
-    if (warp == 0) tmem_alloc(tslot, TM_COLS);
-    tc_fence_before();
+    // longest consumer sequence: tasks beyond it do not exist
+    if (tid == 0) misc[1] = 0;
     sync_compute();
-    tc_fence_after();
-    const uint32_t tmem = *tslot;
-    const uint32_t tl = tmem + (static_cast<uint32_t>(32 * quad) << 16);  // this warp's lane quarter
-    {  // longest consumer sequence: tasks beyond it do not exist
+    {
         int mx = 0;
         for (int k = tid; k < p.C; k += NCOMP) mx = max(mx, consumer_total(p, smem, cu_s, k));
         atomicMax(&misc[1], mx);
+    }
+    // the upper 16x16 tiles of scale*Aqk are never written: zero them once
+    for (int idx = tid; idx < 6 * 16 * 8; idx += NCOMP) {
+        const int tile = idx >> 7, rr = (idx >> 3) & 15, cc = (idx & 7) << 1;
+        const int i = tile < 3 ? 0 : (tile < 5 ? 1 : 2);
+        const int j = tile < 3 ? tile + 1 : (tile < 5 ? tile - 1 : 3);
+        *reinterpret_cast<uint32_t *>(smem + OFF_IMG + SL_AQK + tile_elem(64, 16 * i + rr, 16 * j + cc)) = 0u;
     }
     sync_compute();
     const int jmax = misc[1];
@@ -734,351 +954,67 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int pi
     Task cur = get_task(misc + 2);
     Task nxt = get_task(misc + 10);
     sync_compute();
-    if (cur.valid) issue_loads(p, smem, cur, 0, 0, NCOMP);
-    if (tid == REL_TID) misc[21] = cur.valid && slot_free(R, cur, R.spin) ? 1 : 0;  // nothing is unpublished yet
-    const uint32_t idesc_x = umma_idesc_f16(false, false, 128, 64);  // R^T (tensor memory) x T^T (K-major)
-    bool gate_bad = false;
-    float vmax = 0.f;         // largest magnitude sent to an fp16 operand (NaN if any was NaN)
-    Task prev{0, 0, 0, 0, 0, 0, 0, 0};
-    bool x_pending = false;   // prev's WY product is in flight
-    int it = 0;
+    if (cur.valid) issue_loads(p, smem, cur);
+    bool gate_bad = false, range_bad = false;
+    int pending = -1, pending_val = 0;  // REL_TID: the last slot stored but not yet published
     while (cur.valid) {
-        const int bb = it & 1;  // beta and R^T buffers of this task
-        const float *sBeta = reinterpret_cast<const float *>(smem + OFF_BETA + 256 * bb);
         KDA_TRACE_EV(p, 1, cur.j * p.C + cur.k);
         cp_async_wait_group1();  // g (q, k, v and beta may still be in flight)
         sync_compute();
-        // ---- step 1: inclusive prefix sum of g (base 2) over the sub-block's 16
-        // tokens in registers, then the sub-block carries through shared memory
-        float G[16];
-        {
-            float x[16];
-#pragma unroll
-            for (int r = 0; r < 16; ++r) x[r] = *reinterpret_cast<const float *>(smem + OFF_G + g_elem(16 * blk + r, chn));
-            if (p.raw) {  // g = lower_bound * sigmoid(e^A_log (g_raw + dt_bias)); rows past the sequence end stay 0
-                const float *gp = reinterpret_cast<const float *>(smem + OFF_GPAR);
-                const float a = __expf(gp[128]), db = gp[chn];
-#pragma unroll
-                for (int r = 0; r < 16; ++r)
-                    x[r] = (16 * blk + r < cur.nv) ? __fdividef(p.lb, 1.f + __expf(-a * (x[r] + db))) : 0.f;
-            }
-            float acc = 0.f;
-            bool gb = false;
-#pragma unroll
-            for (int r = 0; r < 16; ++r) {
-                gb |= !(x[r] >= p.lb && x[r] <= 0.f);
-                acc += x[r] * LOG2E;
-                G[r] = acc;
-            }
-            gate_bad |= gb;
-            sTot[blk * 128 + chn] = acc;
-        }
-        cp_async_wait_all();  // q, k, v and beta
-        sync_compute();
-        if (p.raw && tid < BT) {  // beta = sigmoid(beta_raw); rows past the sequence end stay 0
-            float *bw = reinterpret_cast<float *>(smem + OFF_BETA + 256 * bb);
-            bw[tid] = tid < cur.nv ? __fdividef(1.f, 1.f + __expf(-bw[tid])) : 0.f;
-        }
-        float Gl = 0.f;
-        {
-            float carry = 0.f;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float t = sTot[q * 128 + chn];
-                if (q < blk) carry += t;
-                Gl += t;
-            }
-#pragma unroll
-            for (int r = 0; r < 16; ++r) G[r] += carry;
-        }
-        const float Gm = G[7];  // the sub-block midpoint (rows past the end carry the last valid prefix)
-        sGm[blk * 128 + chn] = Gm;
-        sync_compute();
-        for (int j = 0; j < blk; ++j) sF[f_pair(blk, j) * 128 + chn] = ex2(Gm - sGm[j * 128 + chn]);
         KDA_TRACE_EV(p, 20, 0);
-
-        // ---- steps 2a/4a: elementwise products of the thread's 16 tokens:
-        // strip operands into shared memory, R^T into tensor memory, q_hat and
-        // kg into registers (they go to the slot once it is known to be free)
-        uint32_t qh[8], kgp[8];
-        {
-            const float EM = ex2(Gm), EMs = scale * EM, EL = ex2(Gl - Gm);
-            float bt[16];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float4 b4 = reinterpret_cast<const float4 *>(sBeta)[4 * blk + q];
-                bt[4 * q] = b4.x; bt[4 * q + 1] = b4.y; bt[4 * q + 2] = b4.z; bt[4 * q + 3] = b4.w;
-            }
-            uint32_t rv[8], rk[8];
-            float vm = 0.f;
-#pragma unroll
-            for (int r2 = 0; r2 < 8; ++r2) {
-                float oq[2], ok[2], ov[2], orr[2];
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int r = 2 * r2 + e, t = 16 * blk + r;
-                    const int te = tile_elem(64, t, chn);
-                    const float qf = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(smem + OFF_Q + te));
-                    const float kf = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(smem + OFF_K + te));
-                    const float vf = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(smem + OFF_V + te));
-                    const float x = G[r] - Gm;
-                    const float a = ex2(x), b = ex2(-x);
-                    const float qa = qf * a, ka = kf * a, kb = kf * b;
-                    *reinterpret_cast<uint32_t *>(smem + OFF_QA + qa_pair(t, chn) + 4 * (chn & 1)) = tf32_rna(qa);
-                    *reinterpret_cast<__nv_bfloat16 *>(smem + OFF_KA + te) = __float2bfloat16_rn(ka);
-                    sKB[t * RSF + chn] = kb;
-                    oq[e] = qa * EMs;           // scale q e^G
-                    ok[e] = kb * EL;            // k e^(G_last - G)
-                    ov[e] = bt[r] * vf;         // beta v
-                    orr[e] = bt[r] * (ka * EM); // beta k e^G
-                    vm = max_abs_nan(max_abs_nan(vm, oq[e]), ok[e]);
-                    vm = max_abs_nan(max_abs_nan(vm, ov[e]), orr[e]);
-                }
-                qh[r2] = pack_f16(oq[0], oq[1]);
-                kgp[r2] = pack_f16(ok[0], ok[1]);
-                rv[r2] = pack_f16(ov[0], ov[1]);
-                rk[r2] = pack_f16(orr[0], orr[1]);
-            }
-            vmax = max_abs_nan(vmax, vm);
-            tmem_st8(tl + TM_RV + 32 * bb + 8 * blk, rv);
-            tmem_st8(tl + TM_RK + 32 * bb + 8 * blk, rk);
-            tmem_wait_st();
+        Task nxt2{0, 0, 0, 0, 0, 0, 0, 0};
+        if (!run_task(p, R, smem, cur, cu_s, jmax, nxt, nxt2, cs, pending, pending_val, gate_bad, range_bad))
+            break;
+        if (tid == REL_TID) {
+            pending = cur.k * RING + cur.j % RING;
+            pending_val = cur.j + 1;
         }
-        const bool fast = misc[21] != 0;  // written during the previous task's strips
-        tc_fence_before();
-        sync_compute();  // input tiles consumed; strip operands and tables in place
-        KDA_TRACE_EV(p, 21, 0);
-        // Is this task's slot known to be free (checked during the previous task)?
-        // If so, the previous task's WY product is read out and its slot published
-        // by warps 10-13 while the strips run. Otherwise every warp reads it out
-        // now, the slot is published, and only then is this task's slot awaited,
-        // so that no producer waits for a consumer while it holds an unpublished chunk.
-        if (!fast) {
-            if (x_pending) {
-                wait_local(R, bar_x, (it - 1) & 1, p.status);
-                tc_fence_after();
-                read_out_x(tl, slot_of(R, prev), chn, blk, blk + 1, vmax);
-                x_pending = false;
-            }
-            tc_fence_before();
-            sync_compute();  // every write of the previous slot issued; X^T read out
-            if (tid == REL_TID) {
-                if (prev.valid) publish(p, R, prev);
-                const bool ok = slot_free(R, cur, R.spin);
-                if (!ok) {
-                    set_status(p.status, KDA_ERR_TIMEOUT);
-                    atomicExch(&R.hdr->abort, 1);
-                }
-                misc[20] = ok ? 1 : 0;
-            }
-            sync_compute();
-            if (!misc[20]) break;
-            prev.valid = 0;
-        }
-        KDA_TRACE_EV(p, 22, 0);
-        unsigned char *dst = slot_of(R, cur);
-        st_row32(dst + SL_B1, 128, chn, 16 * blk, qh);
-        st_row32(dst + SL_B23, 192, chn, 16 * blk, kgp);
-        if (blk == 0) reinterpret_cast<float *>(dst + SL_D)[chn] = ex2(Gl);
-
-        // ---- step 2b: Aqk and Akk on the 10 lower 16x16 tiles in four groups,
-        // warps 0-3 (one per sub-partition): rows {0,1} x columns {0,1},
-        // rows {2,3} x column 0, rows {2,3} x column 1, rows {2,3} x columns {2,3}
-        static_assert(NWARPS == 16, "warps 0-3 strips, 4-9 next inputs, 10-13 WY read-out, 14-15 diagonal inverses");
-        if (warp < 4) {
-            if (warp == 0) strip_group<0, 0, 2>(smem, dst, sBeta, scale, lane);
-            else if (warp == 1) strip_group<2, 0, 1>(smem, dst, sBeta, scale, lane);
-            else if (warp == 2) strip_group<2, 1, 1>(smem, dst, sBeta, scale, lane);
-            else strip_group<2, 2, 2>(smem, dst, sBeta, scale, lane);
-            if (warp == 0 || warp == 3) {  // the diagonal blocks of L are in place: hand them to the inverse warps
-                __syncwarp();
-                named_bar_arrive(2, 128);
-            }
-            if (lane == 0) KDA_TRACE_ANY(p, 40 + warp, 0);
-        }
-        // ---- warps 4-9: the next task's inputs (the input tiles are free) and its draw
-        if (warp >= 4 && warp < 10) {
-            if (tid == SYNC_TID) {
-                const Task t = fetch_task(p, smem, cu_s, jmax, cs);
-                put_task(misc + 2, t);
-            }
-            if (nxt.valid) issue_loads(p, smem, nxt, bb ^ 1, 4 * 32, 6 * 32);
-        }
-        // ---- step 3a, on warps 14 and 15 (two blocks each, 16 lanes per block)
-        // while the strips run: T_ii = (I + L_ii)^-1 by fp32 forward substitution,
-        // once the four warps with the diagonal tiles have written them
-        if (warp >= 14) {
-            named_bar_sync(2, 128);
-            const int i = 2 * (warp - 14) + (lane >> 4), jc = lane & 15;
-            const float *Ld = sLD + i * 16 * 17;
-            float x[16];
-#pragma unroll
-            for (int r = 0; r < 16; ++r) {
-                float sacc = (r == jc) ? 1.f : 0.f;
-#pragma unroll
-                for (int cc = 0; cc < r; ++cc) sacc -= Ld[r * 17 + cc] * x[cc];
-                x[r] = sacc;
-            }
-            float vm = 0.f;
-#pragma unroll
-            for (int r = 0; r < 16; ++r) {
-                vm = max_abs_nan(vm, x[r]);
-                *reinterpret_cast<__half *>(sT + tile_elem(64, 16 * i + r, 16 * i + jc)) = __float2half_rn(x[r]);
-            }
-            vmax = max_abs_nan(vmax, vm);
-            if (lane == 0) KDA_TRACE_ANY(p, 50 + warp - 14, 0);
-        }
-        // ---- warps 10-13 (one per lane quarter): the previous task's WY product
-        // into its slot, then its publication; and whether the next task's slot
-        // is free: one flag load, issued first and completed by the publication's
-        // fence (an acquire), so that nothing here waits on a consumer
-        if (warp >= 10 && warp < 14) {
-            const bool need_check = nxt.valid && nxt.j >= RING;
-            int fr = 0;
-            if (tid == REL_TID && need_check) fr = ld_relaxed(&R.freed[nxt.k * RING + nxt.j % RING]);
-            if (x_pending) {
-                wait_local(R, bar_x, (it - 1) & 1, p.status);
-                tc_fence_after();
-                read_out_x(tl, slot_of(R, prev), chn, 0, 4, vmax);
-            }
-            if (cur.j < RING) {  // the first use of this slot: the tiles of Aqk above the diagonal are zero
-                for (int idx = tid - 10 * 32; idx < 6 * 16 * 2; idx += 128) {
-                    const int tile = idx >> 5, rr = (idx >> 1) & 15, half = idx & 1;
-                    const int i = tile < 3 ? 0 : (tile < 5 ? 1 : 2);
-                    const int j = tile < 3 ? tile + 1 : (tile < 5 ? tile - 1 : 3);
-                    *reinterpret_cast<uint4 *>(dst + SL_B23 + tile_chunk(192, 128 + 16 * i + rr, 16 * j + 8 * half)) =
-                        make_uint4(0, 0, 0, 0);
-                }
-            }
-            named_bar_sync(6, 128);
-            if (tid == REL_TID) {
-                if (x_pending && prev.valid)
-                    publish(p, R, prev);
-                else if (need_check)
-                    fence_acq_rel_gpu();
-                misc[21] = (nxt.valid && (!need_check || fr >= nxt.j - RING + 1)) ? 1 : 0;
-                KDA_TRACE_ANY(p, 29, 0);
-            }
-        }
-        sync_compute();
-        x_pending = false;
-        const Task nxt2 = get_task(misc + 2);  // drawn after the elementwise step
-        KDA_TRACE_EV(p, 23, 0);
-
-        // ---- step 3b: the block diagonals d = 1, 2, 3 of T = (I + L)^-1,
-        // T_ij = -T_ii * sum_{k=j}^{i-1} L_ik T_kj, one block per warp
-#pragma unroll
-        for (int d = 1; d < 4; ++d) {
-            if (warp < 4 - d) {
-                const int j = warp, i = warp + d;
-                float m[2][4] = {};
-                for (int kb = j; kb < i; ++kb) {
-                    uint32_t fa[4], fb[4];
-                    ldsm_x4(fa, sL + (16 * i + (lane & 15)) * RSA + 16 * kb + ((lane >> 4) << 3));
-                    ldsm_x4_t(fb, sT + bk_addr(lane, 64, 16 * kb, 16 * j));
-                    mma16816_f16(m[0], fa, fb[0], fb[1]);
-                    mma16816_f16(m[1], fa, fb[2], fb[3]);
-                }
-                float vm = 0.f;
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int hf = 0; hf < 2; ++hf) {
-                        vm = max_abs_nan(max_abs_nan(vm, m[nt][2 * hf]), m[nt][2 * hf + 1]);
-                        *reinterpret_cast<uint32_t *>(sT + tile_elem(64, 16 * i + gq + 8 * hf, 16 * j + 8 * nt + 2 * qd)) =
-                            pack_f16(m[nt][2 * hf], m[nt][2 * hf + 1]);
-                    }
-                __syncwarp();
-                float t[2][4] = {};
-                {
-                    uint32_t fa[4], fb[4];
-                    ldsm_x4(fa, sT + a_addr(lane, 64, 16 * i, 16 * i));
-                    ldsm_x4_t(fb, sT + bk_addr(lane, 64, 16 * i, 16 * j));
-                    mma16816_f16(t[0], fa, fb[0], fb[1]);
-                    mma16816_f16(t[1], fa, fb[2], fb[3]);
-                }
-                __syncwarp();
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int hf = 0; hf < 2; ++hf) {
-                        vm = max_abs_nan(max_abs_nan(vm, t[nt][2 * hf]), t[nt][2 * hf + 1]);
-                        *reinterpret_cast<uint32_t *>(sT + tile_elem(64, 16 * i + gq + 8 * hf, 16 * j + 8 * nt + 2 * qd)) =
-                            pack_f16(-t[nt][2 * hf], -t[nt][2 * hf + 1]);
-                    }
-                vmax = max_abs_nan(vmax, vm);
-            }
-            if (d < 3) sync_compute();
-        }
-        // ---- step 4b: X^T = R^T T^T = [u | w]^T on the tensor cores (A operands
-        // in tensor memory), read out during the next task
-        fence_proxy_async_shared();  // T's generic writes, before the tensor core reads it
-        tc_fence_before();
-        sync_compute();
-        KDA_TRACE_EV(p, 24, 0);
-        if (tid == 0) {
-            tc_fence_after();
-            const uint32_t tb = smem_u32(sT);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-                umma_f16_ts(tmem + TM_XU, tmem + TM_RV + 32 * bb + 8 * kk, umma_desc_sw128(tb + kk * 32, 16, 1024), idesc_x,
-                            kk > 0);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-                umma_f16_ts(tmem + TM_XW, tmem + TM_RK + 32 * bb + 8 * kk, umma_desc_sw128(tb + kk * 32, 16, 1024), idesc_x,
-                            kk > 0);
-            umma_commit(bar_x);
-        }
-        x_pending = true;
-        prev = cur;
-        ++it;
         KDA_TRACE_EV(p, 3, cur.j * p.C + cur.k);
         cur = nxt;
         nxt = nxt2;
     }
-    // the last task's WY product: read out, then publish its slot
-    if (x_pending) {
-        wait_local(R, bar_x, (it - 1) & 1, p.status);
-        tc_fence_after();
-        read_out_x(tl, slot_of(R, prev), chn, blk, blk + 1, vmax);
-        tc_fence_before();
-        sync_compute();
-        if (tid == REL_TID) publish(p, R, prev);
+    if (tid == REL_TID) {
+        bulk_wait_all();
+        if (pending >= 0) {
+            fence_proxy_async_global();
+            if (!(p.debug & KDA_DEBUG_WITHHOLD_READY)) st_release(&R.ready[pending], pending_val);
+        }
     }
     cp_async_wait_all();
     if (gate_bad) set_status(p.status, KDA_ERR_GATE_RANGE);
-    if (!(vmax < F16_SAFE)) set_status(p.status, KDA_ERR_VALUE_RANGE);
-    tc_fence_before();
-    sync_compute();
-    tc_fence_after();
-    if (warp == 0) tmem_dealloc(tmem, TM_COLS);
+    if (range_bad) set_status(p.status, KDA_ERR_VALUE_RANGE);
 }
 }  // namespace prod
 
 // ================================================================== consumer
-// Step 5 on the 5th-generation tensor cores, on the transposed state: tensor
-// memory holds S^T (fp32, lane = value column j, column = key channel c), next
-// to it D^T = [q_hat S ; w S]^T (columns 128-191: tokens of q_hat S, which
-// become o^T; 192-255: tokens of w S), and the two fp16 A operands of the
-// chunk, S16^T and v_new^T. One thread issues the products; warp w serves lanes
-// 32 (w % 4) .. + 31 (value columns), key columns 32 (w / 4) .. + 31 of S^T and
-// tokens 16 (w / 4) .. + 15 of D^T.
-//   MMA1   D^T  = S16^T (tensor memory, 128 x 128) * [q_hat ; w]^T (MN-major)
-//   MMA23  [S^T | o^T] += v_new^T (tensor memory, 128 x 64) * [kg^T ; Aqk]
-//          (K-major, N = 192), after S^T <- S^T Diag(d)
-// Only E1 (the fp16 copy of S^T), MMA1, E2 (v_new) and MMA23 are on the chain;
-// the decay and the previous chunk's o rows are done while MMA1 runs.
+// Step 5 on the 5th-generation tensor cores. TMEM holds the fp32 state S
+// (columns 0-127, lane = key channel) and the accumulator D = [q_hat S ; w S]
+// (columns 128-255, lanes 0-63 = tokens of q_hat S, lanes 64-127 = tokens of
+// w S). One thread issues the MMAs; all sixteen warps run the epilogues, warp w
+// on TMEM lanes 32*(w%4).. and value columns 32*(w/4)..
+//   MMA1  D  = [q_hat ; w] (K-major, 128 x 128) * S16 (fp16 snapshot, MN-major)
+//   MMA2  D += [scale*Aqk ; 0] (K-major, 128 x 64) * v_new (MN-major)   (lanes 0-63: o)
+//   MMA3  S += kg^T (MN-major, 128 x 64) * v_new, after S <- Diag(d) S in TMEM
 namespace cons {
+constexpr int BUF_BYTES = SLOT_BYTES + 8192;   // slot + 8 KB of zeros: rows 64-127 of [Aqk; 0]
 constexpr int OFF_BUF0 = 0;
-constexpr int OFF_BUF1 = SLOT_BYTES;            // 1024-aligned
-constexpr int OFF_RED = 2 * SLOT_BYTES;         // gated norm: per-quarter row sums [4][64], then 1/rms [64]
-constexpr int OFF_BAR = OFF_RED + 1280;         // full[2], mma1, mma23
+constexpr int OFF_BUF1 = BUF_BYTES;             // 82944 (1024-aligned)
+constexpr int OFF_S = 2 * BUF_BYTES;            // S16: fp16 [key][value], MN-major swizzled, 32 KB
+constexpr int OFF_VN = OFF_S + 32768;           // v_new: fp16 [token][value], MN-major swizzled, 16 KB
+constexpr int OFF_BAR = OFF_VN + 16384;         // full[2], mma1, mma23
 constexpr int OFF_TMEM = OFF_BAR + 32;          // TMEM base address written by tcgen05.alloc
 constexpr int OFF_MISC = OFF_BAR + 64;
 constexpr int SMEM = OFF_MISC + 64;
-constexpr uint32_t TM_S = 0, TM_DQ = 128, TM_DW = 192, TM_S16 = 256, TM_VN = 320, TM_COLS = 512;
-static_assert(SLOT_BYTES % 1024 == 0, "slot buffers are 1024-byte aligned");
+constexpr uint32_t TMEM_COLS = 256;
+constexpr int OST = 132;  // fp32 row stride of the o staging tile (64 x OST spans S16 + v_new); columns
+                          // 128-131 hold the row's four slice sums of squares for the gated norm
+static_assert(64 * OST * 4 <= 32768 + 16384, "o staging fits in the state and v_new tiles");
+__device__ __forceinline__ bool f16_ok(float x) { return fabsf(x) < F16_SAFE; }
 
+// one 128-byte line of global memory towards L2 (no register result)
+__device__ __forceinline__ void prefetch_l2(const void *ptr) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
+}
 // logistic function of a bf16 pair, as an fp16 pair: 1/2 + tanh(x/2)/2 with the
 // packed fp16 hardware tanh (one special-function operation per pair; absolute
 // error about 1e-3)
@@ -1091,88 +1027,32 @@ __device__ __forceinline__ uint32_t sigmoid_bf16x2_to_f16x2(uint32_t g2) {
     return r;
 }
 
-// The o rows of one chunk (first token t0, nv valid rows, head h) from this
-// thread's slice of o^T: value column jv, tokens 16 cg .. 16 cg + 15. Each warp
-// store writes 32 consecutive value columns of one row (128 contiguous bytes).
-// With the fused gated RMSNorm, the rows' sums of squares are reduced over the
-// warp's 32 columns (a butterfly that leaves lane l with the sum of token
-// T(l)), then over the four column quarters in shared memory; called by all
-// threads together (it holds two CTA barriers).
-__device__ __forceinline__ void store_o(const Params &p, unsigned char *smem, const uint32_t (&ov)[16], int64_t t0, int nv,
-                                        int h, int jv, int cg, int lane, int quad, const uint32_t (&gt)[8], float nw,
-                                        int e0 = 0, int e1 = 16) {
-    const int tid = threadIdx.x;
-    float x[16];
-#pragma unroll
-    for (int e = 0; e < 16; ++e) x[e] = __uint_as_float(ov[e]);
-    if (p.ngate) {
-        float v[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) v[e] = x[e] * x[e];
-#pragma unroll
-        for (int w = 16, n = 8; w >= 2; w >>= 1, n >>= 1) {  // halve the values held, pairing lanes l and l ^ w
-            const bool up = (lane & w) != 0;
-#pragma unroll
-            for (int e = 0; e < n; ++e) {
-                const float send = up ? v[e] : v[e + n];
-                const float keep = up ? v[e + n] : v[e];
-                v[e] = keep + __shfl_xor_sync(0xffffffffu, send, w);
-            }
-        }
-        v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
-        const int tok = ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
-        float *red = reinterpret_cast<float *>(smem + OFF_RED);
-        if ((lane & 1) == 0) red[quad * 64 + 16 * cg + tok] = v[0];
-        sync_compute();
-        if (tid < BT)
-            red[256 + tid] = rsqrtf(((red[tid] + red[64 + tid]) + (red[128 + tid] + red[192 + tid])) * (1.f / DV) + p.neps);
-        sync_compute();
-        float rs[16];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const float4 r4 = reinterpret_cast<const float4 *>(red + 256 + 16 * cg)[q];
-            rs[4 * q] = r4.x; rs[4 * q + 1] = r4.y; rs[4 * q + 2] = r4.z; rs[4 * q + 3] = r4.w;
-        }
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const float2 sg = unpack_f16(sigmoid_bf16x2_to_f16x2(gt[e]));
-            x[2 * e] *= rs[2 * e] * nw * sg.x;
-            x[2 * e + 1] *= rs[2 * e + 1] * nw * sg.y;
-        }
+// completion of this CTA's own MMAs: depends on no other CTA, so only a
+// (bounded) timeout ends it early, never the abort word
+__device__ __forceinline__ bool wait_all(const Ring &R, uint64_t *bar, uint32_t parity, int32_t *status) {
+    for (long long it = 0; it < SPIN_LIMIT; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
     }
-    if (p.o) {
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-            const int t = 16 * cg + e;
-            if (e >= e0 && e < e1 && t < nv) p.o[(static_cast<size_t>(t0 + t) * p.H + h) * DV + jv] = x[e];
-        }
-    }
-}
-
-// the gate values of this thread's o slice (tokens 16 cg .. + 15 of column jv),
-// as bf16 pairs of consecutive tokens (zero past the chunk's valid rows)
-__device__ __forceinline__ void load_gate(const Params &p, uint32_t (&gt)[8], int64_t t0, int nv, int h, int jv, int cg) {
-    const unsigned short *gp = reinterpret_cast<const unsigned short *>(p.ngate);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        const int t = 16 * cg + 2 * e;
-        const uint32_t lo = t < nv ? __ldg(gp + (static_cast<size_t>(t0 + t) * p.H + h) * DV + jv) : 0u;
-        const uint32_t hi = t + 1 < nv ? __ldg(gp + (static_cast<size_t>(t0 + t + 1) * p.H + h) * DV + jv) : 0u;
-        gt[e] = lo | (hi << 16);
-    }
+    set_status(status, KDA_ERR_TIMEOUT);
+    atomicExch(&R.hdr->abort, 1);
+    return false;
 }
 
 __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int quad = warp & 3, cg = warp >> 2;  // TMEM lane quarter; key-column / token group
-    const int jv = 32 * quad + lane;            // this thread's value column (TMEM lane)
+    const int quad = warp & 3, slice = warp >> 2;  // TMEM lane quarter, 32-column value slice
+    const int row = 32 * quad + lane;             // this thread's TMEM lane
     Ring R = ring_of(p);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
     uint64_t *bar_mma1 = full + 2;
     uint64_t *bar_mma23 = full + 3;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + OFF_TMEM);
     int *misc = reinterpret_cast<int *>(smem + OFF_MISC);
+    unsigned char *sS = smem + OFF_S;
+    unsigned char *sVN = smem + OFF_VN;
 
+    for (int i = tid; i < 2 * 512; i += NCOMP)  // the two zero blocks
+        *reinterpret_cast<uint4 *>(smem + (i >> 9) * BUF_BYTES + SLOT_BYTES + (i & 511) * 16) = make_uint4(0, 0, 0, 0);
     if (tid == 0) {
         mbar_init(&full[0], 1);
         mbar_init(&full[1], 1);
@@ -1181,12 +1061,14 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
         mbar_fence_init();
         misc[0] = 1;
     }
-    if (warp == 0) tmem_alloc(tslot, TM_COLS);
+    if (warp == 0) tmem_alloc(tslot, TMEM_COLS);
+    fence_proxy_async_shared();
     tc_fence_before();
     sync_compute();
     tc_fence_after();
     const uint32_t tmem = *tslot;
-    const uint32_t tl = tmem + (static_cast<uint32_t>(32 * quad) << 16);  // this warp's lane quarter
+    const uint32_t tS = tmem + (static_cast<uint32_t>(32 * quad) << 16) + 32 * slice;  // this thread's S columns
+    const uint32_t tD = tS + 128;                                                       // this thread's D columns
     const int32_t *cu_s = sched_cu(p, smem);
     const int total = consumer_total(p, smem, cu_s, k);
 
@@ -1204,17 +1086,12 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
         else
             misc[0] = 0;
     }
-    const uint32_t idesc1 = umma_idesc_f16(false, true, 128, 128);    // S16^T x [q_hat; w]^T (MN-major)
-    const uint32_t idesc23 = umma_idesc_f16(false, false, 128, 192);  // v_new^T x [kg^T; Aqk] (K-major)
-    const float nw = p.ngate ? __ldg(p.nweight + jv) : 0.f;
+    const uint32_t idesc_qw = umma_idesc_f16(false, true, 128, 128);  // [q_hat; w] x S16
+    const uint32_t idesc_av = umma_idesc_f16(false, true, 128, 128);  // [Aqk; 0] x v_new
+    const uint32_t idesc_kv = umma_idesc_f16(true, true, 128, 128);   // kg^T x v_new
 
-    int jj = 0, n23 = 0;
-    float vmax = 0.f;  // largest magnitude sent to an fp16 operand (NaN if any was NaN)
-    bool alive = true;
-    bool pend = false;  // o^T of the chunk (pt0, pnv, ph) waits in D^T to be stored
-    int64_t pt0 = 0;
-    int pnv = 0, ph = 0;
-    uint32_t gt[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    int j = 0;
+    bool range_bad = false, alive = true;
     const int nchains = sched_count(p, smem, k);
     for (int r = 0; r < nchains && alive; ++r) {
         const int ch = sched_chain(p, smem, k, r);
@@ -1225,203 +1102,263 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
             continue;
         }
         const int n = ch / p.H, h = ch % p.H;
-        const size_t state_base = (static_cast<size_t>(n) * p.H + h) * (DK * DV);
-        // entry state (or zeros) -> S^T: lane jv, key columns 32 cg .. + 31 (each
-        // warp load reads 32 consecutive value columns of one key row)
+        const bool st_inb = checked(ch >= 0 && n < p.N, p.status);  // a failed check skips the state accesses
+        const size_t state_base = st_inb ? (static_cast<size_t>(n) * p.H + h) * (DK * DV) : 0;
+        // initial state (or zeros) -> TMEM: row `row`, columns 32*slice..+31
 #pragma unroll
         for (int cb = 0; cb < 2; ++cb) {
-            uint32_t s[16];
+            uint32_t r[16];
+            if (p.s0 && st_inb) {
+                const float4 *src = reinterpret_cast<const float4 *>(p.s0 + state_base + row * DV + 32 * slice + 16 * cb);
 #pragma unroll
-            for (int e = 0; e < 16; ++e)
-                s[e] = p.s0 ? __float_as_uint(__ldg(p.s0 + state_base + static_cast<size_t>(32 * cg + 16 * cb + e) * DV + jv))
-                            : 0u;
-            tmem_st16(tl + TM_S + 32 * cg + 16 * cb, s);
+                for (int e = 0; e < 4; ++e) {
+                    const float4 f = src[e];
+                    r[4 * e] = __float_as_uint(f.x); r[4 * e + 1] = __float_as_uint(f.y);
+                    r[4 * e + 2] = __float_as_uint(f.z); r[4 * e + 3] = __float_as_uint(f.w);
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 16; ++e) r[e] = 0u;
+            }
+            tmem_st16(tS + 16 * cb, r);
         }
         tmem_wait_st();
 
-        for (int c = 0; c < nc; ++c, ++jj) {
-            const int b = jj & 1;
+        for (int c = 0; c < nc; ++c, ++j) {
+            const int b = j & 1;
             const int64_t t0 = bos + static_cast<int64_t>(c) * BT;
-            const int nv = static_cast<int>((bos + len - t0) < BT ? (bos + len - t0) : BT);
-            KDA_TRACE_EV(p, 10, jj);
-            if (c > 0) {  // the previous chunk's MMA23: S^T and its o^T are final, its buffer is free
-                wait_local(R, bar_mma23, (n23 - 1) & 1, p.status);
-                tc_fence_after();
-            }
-            // (1) slot jj has landed: release its ring slot, start fetching slot jj + 1
+            const int nv_c = static_cast<int>((bos + len - t0) < BT ? (bos + len - t0) : BT);
+            // output rows [t0, t0 + nv); a failed index check writes none of them
+            const int nv = checked(t0 >= 0 && nv_c >= 0 && t0 + nv_c <= p.Ttok, p.status) ? nv_c : 0;
+            KDA_TRACE_EV(p, 10, j);
+            // (1) slot j has landed: release its ring slot, start fetching slot j + 1
             if (tid == 0) {
-                const bool was_alive = misc[0] != 0;  // then slot jj's copy has been issued
-                if (was_alive && wait_mbar(R, &full[b], (jj >> 1) & 1, p.status)) {
-                    // the copy of slot jj has completed (its reads are done): free the
+                const bool was_alive = misc[0] != 0;  // then slot j's copy has been issued
+                if (was_alive && wait_mbar(R, &full[b], (j >> 1) & 1, p.status)) {
+                    // the copy of slot j has completed (its reads are done): free the
                     // slot without ordering this thread's pending o stores before it
-                    st_relaxed(&R.freed[k * RING + jj % RING], jj + 1);
+                    st_relaxed(&R.freed[k * RING + j % RING], j + 1);
                     issued_next = false;
-                    if (jj + 1 < total && ld_acquire(&R.ready[k * RING + (jj + 1) % RING]) >= jj + 2) {
-                        issue(jj + 1);
+                    if (j + 1 < total && ld_acquire(&R.ready[k * RING + (j + 1) % RING]) >= j + 2) {
+                        issue(j + 1);
                         issued_next = true;
+                        KDA_TRACE_ANY(p, 17, j + 1);
                     }
                 } else {
-                    if (was_alive) drain_mbar(&full[b], (jj >> 1) & 1);  // let it land before leaving
+                    if (was_alive) drain_mbar(&full[b], (j >> 1) & 1);  // let it land before leaving
                     misc[0] = 0;
                 }
             }
-            if (pend && p.ngate) load_gate(p, gt, pt0, pnv, ph, jv, cg);
             sync_compute();
             if (!misc[0]) {
                 alive = false;
                 break;
             }
-            for (int it = 0; !mbar_try_wait(&full[b], (jj >> 1) & 1); ++it)
+            if (p.ngate && tid < 2 * BT && (tid >> 1) < nv)  // this chunk's gate rows (two lines each) -> L2
+                prefetch_l2(p.ngate + (static_cast<size_t>(t0 + (tid >> 1)) * p.H + h) * DV + 64 * (tid & 1));
+            for (int it = 0; !mbar_try_wait(&full[b], (j >> 1) & 1); ++it)
                 if (it > (1 << 20)) {
                     set_status(p.status, KDA_ERR_TIMEOUT);
                     break;
                 }
             const unsigned char *bb = smem + (b ? OFF_BUF1 : OFF_BUF0);
-            KDA_TRACE_EV(p, 11, jj);
+            KDA_TRACE_EV(p, 11, j);
 
-            // (2) E1: fp16 copy of S^T for MMA1 (and the previous chunk's o^T into registers)
-            uint32_t sa[16], sb[16], ov[16];
-            tmem_ld16(tl + TM_S + 32 * cg, sa);
-            tmem_ld16(tl + TM_S + 32 * cg + 16, sb);
-            if (pend) tmem_ld16(tl + TM_DQ + 16 * cg, ov);
-            tmem_wait_ld();
+            // (2) fp16 snapshot of the entry state for MMA1, then S <- Diag(d) S in TMEM
             {
-                uint32_t hp[16];
-                float vm = 0.f;
+                const float d = reinterpret_cast<const float *>(bb + SL_D)[row];
+                uint32_t r0[16], r1[16];
+                tmem_ld16(tS, r0);
+                tmem_ld16(tS + 16, r1);
+                tmem_wait_ld();
+                auto snap = [&](uint32_t (&r)[16], int cb) {
+                    uint32_t hp[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float a0 = __uint_as_float(sa[2 * e]), a1 = __uint_as_float(sa[2 * e + 1]);
-                    const float b0 = __uint_as_float(sb[2 * e]), b1 = __uint_as_float(sb[2 * e + 1]);
-                    vm = max_abs_nan(max_abs_nan(vm, a0), a1);
-                    vm = max_abs_nan(max_abs_nan(vm, b0), b1);
-                    hp[e] = pack_f16(a0, a1);
-                    hp[8 + e] = pack_f16(b0, b1);
-                }
-                vmax = max_abs_nan(vmax, vm);
-                tmem_st16(tl + TM_S16 + 16 * cg, hp);
+                    for (int e = 0; e < 8; ++e) {
+                        const float x0 = __uint_as_float(r[2 * e]), x1 = __uint_as_float(r[2 * e + 1]);
+                        range_bad |= !(f16_ok(x0) && f16_ok(x1));
+                        hp[e] = pack_f16(x0, x1);
+                    }
+                    const int c8 = 32 * slice + 16 * cb;
+                    *reinterpret_cast<uint4 *>(sS + tile_chunk(128, row, c8)) = make_uint4(hp[0], hp[1], hp[2], hp[3]);
+                    *reinterpret_cast<uint4 *>(sS + tile_chunk(128, row, c8 + 8)) = make_uint4(hp[4], hp[5], hp[6], hp[7]);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * d);
+                };
+                snap(r0, 0);
+                snap(r1, 1);
+                tmem_st16(tS, r0);
+                tmem_st16(tS + 16, r1);
+                tmem_wait_st();
             }
-            tmem_wait_st();
+            fence_proxy_async_shared();
             tc_fence_before();
             sync_compute();
-            // (3) MMA1: D^T = S16^T [q_hat ; w]^T
+            KDA_TRACE_EV(p, 13, j);
+
+            // (3) MMA1: D = [q_hat ; w] S16
             if (tid == 0) {
                 tc_fence_after();
-                const uint32_t b1 = smem_u32(bb + SL_B1);
+                const uint32_t a0 = smem_u32(bb + SL_A1), b0 = smem_u32(sS);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    umma_f16_ts(tmem + TM_DQ, tmem + TM_S16 + 8 * kk, umma_desc_sw128(b1 + kk * 2048, 16384, 1024), idesc1,
-                                kk > 0);
+                    umma_f16(tmem + 128, umma_desc_sw128(a0 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+                             umma_desc_sw128(b0 + kk * 2048, 16384, 1024), idesc_qw, kk > 0);
                 umma_commit(bar_mma1);
             }
-            KDA_TRACE_EV(p, 13, jj);
-            // (4) off the chain while MMA1 runs: S^T <- S^T Diag(d), and the
-            // previous chunk's o rows
-            {
-                const float4 *dp = reinterpret_cast<const float4 *>(bb + SL_D) + 8 * cg;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float4 d0 = dp[q], d1 = dp[4 + q];
-                    sa[4 * q] = __float_as_uint(__uint_as_float(sa[4 * q]) * d0.x);
-                    sa[4 * q + 1] = __float_as_uint(__uint_as_float(sa[4 * q + 1]) * d0.y);
-                    sa[4 * q + 2] = __float_as_uint(__uint_as_float(sa[4 * q + 2]) * d0.z);
-                    sa[4 * q + 3] = __float_as_uint(__uint_as_float(sa[4 * q + 3]) * d0.w);
-                    sb[4 * q] = __float_as_uint(__uint_as_float(sb[4 * q]) * d1.x);
-                    sb[4 * q + 1] = __float_as_uint(__uint_as_float(sb[4 * q + 1]) * d1.y);
-                    sb[4 * q + 2] = __float_as_uint(__uint_as_float(sb[4 * q + 2]) * d1.z);
-                    sb[4 * q + 3] = __float_as_uint(__uint_as_float(sb[4 * q + 3]) * d1.w);
-                }
-                tmem_st16(tl + TM_S + 32 * cg, sa);
-                tmem_st16(tl + TM_S + 32 * cg + 16, sb);
-            }
-            KDA_TRACE_EV(p, 15, jj);
-            // the first half of the previous chunk's o rows (the other half is stored
-            // while MMA23 runs; with the gated norm all of them are, then)
-            if (pend && !p.ngate) store_o(p, smem, ov, pt0, pnv, ph, jv, cg, lane, quad, gt, nw, 0, 8);
-            tmem_wait_st();
-            KDA_TRACE_EV(p, 16, jj);
 
-            // (5) E2: v_new^T = u^T - (w S)^T -> fp16 A operand of MMA23
-            wait_local(R, bar_mma1, jj & 1, p.status);
+            // (4) v_new = u - w S (TMEM lanes 64-127) -> fp16 [token][value] tile
+            wait_all(R, bar_mma1, j & 1, p.status);
             tc_fence_after();
-            KDA_TRACE_EV(p, 14, jj);
-            {
-                uint32_t dw[16];
-                tmem_ld16(tl + TM_DW + 16 * cg, dw);
-                const uint4 u0 = *reinterpret_cast<const uint4 *>(bb + SL_U + tile_chunk(128, jv, 16 * cg));
-                const uint4 u1 = *reinterpret_cast<const uint4 *>(bb + SL_U + tile_chunk(128, jv, 16 * cg + 8));
-                const uint32_t uw[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+            KDA_TRACE_EV(p, 14, j);
+            if (quad >= 2) {
+                const int t = row - 64;
+                uint32_t r0[16], r1[16];
+                tmem_ld16(tD, r0);
+                tmem_ld16(tD + 16, r1);
                 tmem_wait_ld();
-                uint32_t vp[8];
-                float vm = 0.f;
+                auto vnew = [&](const uint32_t (&r)[16], int cb) {
+                    const int c8 = 32 * slice + 16 * cb;
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float2 u2 = unpack_f16(uw[e]);
-                    const float y0 = u2.x - __uint_as_float(dw[2 * e]);
-                    const float y1 = u2.y - __uint_as_float(dw[2 * e + 1]);
-                    vm = max_abs_nan(max_abs_nan(vm, y0), y1);
-                    vp[e] = pack_f16(y0, y1);
-                }
-                vmax = max_abs_nan(vmax, vm);
-                tmem_st8(tl + TM_VN + 8 * cg, vp);
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const uint4 uu = *reinterpret_cast<const uint4 *>(bb + SL_U + tile_chunk(64, t, c8 + 8 * hh));
+                        const uint32_t *uw = reinterpret_cast<const uint32_t *>(&uu);
+                        uint32_t vp[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 u2 = unpack_f16(uw[e]);
+                            const float y0 = u2.x - __uint_as_float(r[8 * hh + 2 * e]);
+                            const float y1 = u2.y - __uint_as_float(r[8 * hh + 2 * e + 1]);
+                            range_bad |= !(f16_ok(y0) && f16_ok(y1));
+                            vp[e] = pack_f16(y0, y1);
+                        }
+                        *reinterpret_cast<uint4 *>(sVN + tile_chunk(64, t, c8 + 8 * hh)) = make_uint4(vp[0], vp[1], vp[2], vp[3]);
+                    }
+                };
+                vnew(r0, 0);
+                vnew(r1, 1);
             }
-            tmem_wait_st();
+            fence_proxy_async_shared();
             tc_fence_before();
             sync_compute();
-            // (6) MMA23: [S^T | o^T] += v_new^T [kg^T ; Aqk]
+            KDA_TRACE_EV(p, 15, j);
+
+            // (5) MMA2: D[0:64] += (scale Aqk) v_new ; MMA3: S += kg^T v_new
             if (tid == 0) {
                 tc_fence_after();
-                const uint32_t b23 = smem_u32(bb + SL_B23);
+                const uint32_t aq = smem_u32(bb + SL_AQK), vn = smem_u32(sVN), kg = smem_u32(bb + SL_KG);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    umma_f16_ts(tmem + TM_S, tmem + TM_VN + 8 * kk, umma_desc_sw128(b23 + kk * 32, 16, 1024), idesc23, 1);
+                    umma_f16(tmem + 128, umma_desc_sw128(aq + kk * 32, 16, 1024), umma_desc_sw128(vn + kk * 2048, 8192, 1024),
+                             idesc_av, 1);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    umma_f16(tmem, umma_desc_sw128(kg + kk * 2048, 8192, 1024), umma_desc_sw128(vn + kk * 2048, 8192, 1024),
+                             idesc_kv, 1);
                 umma_commit(bar_mma23);
             }
-            if (pend) store_o(p, smem, ov, pt0, pnv, ph, jv, cg, lane, quad, gt, nw, p.ngate ? 0 : 8, 16);
-            ++n23;
-            pend = true;
-            pt0 = t0;
-            pnv = nv;
-            ph = h;
-            KDA_TRACE_EV(p, 12, jj);
-            if (tid == 0 && !issued_next && jj + 1 < total) {
-                if (wait_flag_geq(R, &R.ready[k * RING + (jj + 1) % RING], jj + 2, p.status))
-                    issue(jj + 1);
+
+            // (6) o (TMEM lanes 0-63) -> staging in the (now free) state/v_new tiles ->
+            // global, one full 512-byte row per warp store. With the fused gated
+            // RMSNorm, warp w stores rows w, w+16, w+32, w+48: their gate values
+            // (this lane's four channels) are loaded before the wait, so that
+            // the loads land while MMA2/MMA3 run and o is staged.
+            static_assert(NCOMP / 32 * 4 == BT, "four output rows per warp");
+            uint2 gv[4];
+            if (p.ngate) {
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    const int rr = warp + 16 * q4;
+                    gv[q4] = rr < nv ? __ldg(reinterpret_cast<const uint2 *>(p.ngate + (static_cast<size_t>(t0 + rr) * p.H + h) * DV) + lane)
+                                     : make_uint2(0u, 0u);
+                }
+            }
+            wait_all(R, bar_mma23, j & 1, p.status);
+            tc_fence_after();
+            KDA_TRACE_EV(p, 16, j);
+            float *stg = reinterpret_cast<float *>(sS);  // [64][OST] fp32, spans the S16 and v_new tiles
+            if (quad < 2) {
+                uint32_t r0[16], r1[16];
+                tmem_ld16(tD, r0);
+                tmem_ld16(tD + 16, r1);
+                tmem_wait_ld();
+                float *dst = stg + row * OST + 32 * slice;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    reinterpret_cast<float4 *>(dst)[e] = make_float4(__uint_as_float(r0[4 * e]), __uint_as_float(r0[4 * e + 1]),
+                                                                     __uint_as_float(r0[4 * e + 2]), __uint_as_float(r0[4 * e + 3]));
+                    reinterpret_cast<float4 *>(dst + 16)[e] = make_float4(__uint_as_float(r1[4 * e]), __uint_as_float(r1[4 * e + 1]),
+                                                                          __uint_as_float(r1[4 * e + 2]), __uint_as_float(r1[4 * e + 3]));
+                }
+                if (p.ngate) {  // this slice's sum of squares of the row, into the row's pad column 128 + slice
+                    float ss = 0.f;
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const float x0 = __uint_as_float(r0[e]), x1 = __uint_as_float(r1[e]);
+                        ss = fmaf(x0, x0, ss);
+                        ss = fmaf(x1, x1, ss);
+                    }
+                    stg[row * OST + DV + slice] = ss;
+                }
+            }
+            tc_fence_before();
+            sync_compute();
+            if (!p.o) {
+                // states only: no output rows
+            } else if (p.ngate) {
+                // y = x / sqrt(mean(x^2) + eps) * weight * sigmoid(gate) over the row's 128 channels
+                const float4 w4 = __ldg(reinterpret_cast<const float4 *>(p.nweight) + lane);
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    const int rr = warp + 16 * q4;
+                    if (rr < nv) {  // uniform in the warp
+                        const float4 x = *reinterpret_cast<const float4 *>(stg + rr * OST + 4 * lane);
+                        const float4 ps = *reinterpret_cast<const float4 *>(stg + rr * OST + DV);  // the four slices' sums
+                        const float rs = rsqrtf(((ps.x + ps.y) + (ps.z + ps.w)) * (1.f / DV) + p.neps);
+                        const float2 sa = unpack_f16(sigmoid_bf16x2_to_f16x2(gv[q4].x));
+                        const float2 sb = unpack_f16(sigmoid_bf16x2_to_f16x2(gv[q4].y));
+                        reinterpret_cast<float4 *>(p.o + (static_cast<size_t>(t0 + rr) * p.H + h) * DV)[lane] =
+                            make_float4(x.x * rs * w4.x * sa.x, x.y * rs * w4.y * sa.y, x.z * rs * w4.z * sb.x,
+                                        x.w * rs * w4.w * sb.y);
+                    }
+                }
+            } else {
+                for (int rr = warp; rr < nv; rr += NCOMP / 32)
+                    reinterpret_cast<float4 *>(p.o + (static_cast<size_t>(t0 + rr) * p.H + h) * DV)[lane] =
+                        *reinterpret_cast<const float4 *>(stg + rr * OST + 4 * lane);
+            }
+            KDA_TRACE_EV(p, 12, j);
+            if (tid == 0 && !issued_next && j + 1 < total) {
+                if (wait_flag_geq(R, &R.ready[k * RING + (j + 1) % RING], j + 2, p.status)) {
+                    issue(j + 1);
+                    KDA_TRACE_ANY(p, 18, j + 1);
+                }
                 else
                     misc[0] = 0;
             }
         }
         if (!alive) break;
-        if (nc > 0) {  // the chain's last o rows
-            wait_local(R, bar_mma23, (n23 - 1) & 1, p.status);
+        // final state: TMEM -> global
+        if (p.sT && st_inb) {
             tc_fence_after();
-            if (p.ngate) load_gate(p, gt, pt0, pnv, ph, jv, cg);
-            uint32_t ov[16];
-            tmem_ld16(tl + TM_DQ + 16 * cg, ov);
-            tmem_wait_ld();
-            store_o(p, smem, ov, pt0, pnv, ph, jv, cg, lane, quad, gt, nw);
-            pend = false;
-        }
-        // final state: S^T -> global (each warp store writes 32 consecutive value columns)
-        if (p.sT) {
 #pragma unroll
             for (int cb = 0; cb < 2; ++cb) {
-                uint32_t s[16];
-                tmem_ld16(tl + TM_S + 32 * cg + 16 * cb, s);
+                uint32_t r[16];
+                tmem_ld16(tS + 16 * cb, r);
                 tmem_wait_ld();
+                float4 *dst = reinterpret_cast<float4 *>(p.sT + state_base + row * DV + 32 * slice + 16 * cb);
 #pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    p.sT[state_base + static_cast<size_t>(32 * cg + 16 * cb + e) * DV + jv] = __uint_as_float(s[e]);
+                for (int e = 0; e < 4; ++e)
+                    dst[e] = make_float4(__uint_as_float(r[4 * e]), __uint_as_float(r[4 * e + 1]),
+                                         __uint_as_float(r[4 * e + 2]), __uint_as_float(r[4 * e + 3]));
             }
         }
-        tc_fence_before();
-        sync_compute();
-        tc_fence_after();
     }
-    if (!(vmax < F16_SAFE)) set_status(p.status, KDA_ERR_VALUE_RANGE);
+    if (range_bad) set_status(p.status, KDA_ERR_VALUE_RANGE);
     tc_fence_before();
     sync_compute();
     tc_fence_after();
-    if (warp == 0) tmem_dealloc(tmem, TM_COLS);
+    if (warp == 0) tmem_dealloc(tmem, TMEM_COLS);
 }
 }  // namespace cons
 

@@ -226,3 +226,16 @@ def test_value_beyond_fp16_operand_range_sets_device_status():
     with pytest.raises(KdaError) as ei:
         pu.run_gpu(inp)
     assert ei.value.code == KDA_ERR_VALUE_RANGE
+
+
+def test_inverse_beyond_fp16_range_sets_device_status():
+    # three equal long keys with beta = 1 and g = 0: L has entries a = |k|^2 = 900 (inside the fp16 range)
+    # while T = (I + L)^-1 has a^2 - a ~ 8e5 in row 2, column 0, beyond it
+    from kda_chunked_prefill_gb300 import KDA_ERR_VALUE_RANGE, KdaError
+    inp = kin.make_inputs([50], 1, seed=17)
+    inp["k"][0:3, 0, :] = (30.0 / 128 ** 0.5)
+    inp["g"][0:3, 0, :] = 0.0
+    inp["beta"][0:3, 0] = 1.0
+    with pytest.raises(KdaError) as ei:
+        pu.run_gpu(inp)
+    assert ei.value.code == KDA_ERR_VALUE_RANGE

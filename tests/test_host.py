@@ -45,7 +45,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_version_and_status_strings(lib):
     assert kda.version() >= 100
-    for code in range(8):
+    for code in range(10):
         assert kda.status_string(code) not in ("", "unknown status")
     assert kda.status_string(99) == "unknown status"
 
