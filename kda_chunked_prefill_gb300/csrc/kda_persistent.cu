@@ -1027,6 +1027,15 @@ __device__ __forceinline__ uint32_t sigmoid_bf16x2_to_f16x2(uint32_t g2) {
     return r;
 }
 
+// 3-D tiled tensor store shared memory -> global (coordinates innermost
+// first), tracked by the issuing thread's bulk async-groups
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, const void *src, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(src))
+                 : "memory");
+}
+
 // completion of this CTA's own MMAs: depends on no other CTA, so only a
 // (bounded) timeout ends it early, never the abort word
 __device__ __forceinline__ bool wait_all(const Ring &R, uint64_t *bar, uint32_t parity, int32_t *status) {
@@ -1072,9 +1081,17 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
     const int32_t *cu_s = sched_cu(p, smem);
     const int total = consumer_total(p, smem, cu_s, k);
 
-    auto issue = [&](int jj) {  // slot jj -> buffer jj % 2 (thread 0)
+    // slot jj -> buffer jj % 2 (thread 0). The buffer last staged the o of
+    // chunk jj - 2 for its tensor stores: they must have read it first.
+    // `newest_elsewhere`: this thread's newest store group staged in the
+    // other buffer and may go on.
+    auto issue = [&](int jj, bool newest_elsewhere) {
         const unsigned char *src = R.slots + static_cast<size_t>(k * RING + jj % RING) * SLOT_BYTES;
         unsigned char *dst = smem + ((jj & 1) ? OFF_BUF1 : OFF_BUF0);
+        if (newest_elsewhere)
+            asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+        else
+            bulk_wait_read();
         fence_proxy_async_global();
         mbar_arrive_expect_tx(&full[jj & 1], SLOT_BYTES);
         bulk_g2s(dst, src, SLOT_BYTES, &full[jj & 1]);
@@ -1082,7 +1099,7 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
     bool issued_next = false;  // thread 0 only
     if (tid == 0 && total > 0) {
         if (wait_flag_geq(R, &R.ready[k * RING], 1, p.status))
-            issue(0);
+            issue(0, false);
         else
             misc[0] = 0;
     }
@@ -1139,8 +1156,11 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
                     // slot without ordering this thread's pending o stores before it
                     st_relaxed(&R.freed[k * RING + j % RING], j + 1);
                     issued_next = false;
-                    if (j + 1 < total && ld_acquire(&R.ready[k * RING + (j + 1) % RING]) >= j + 2) {
-                        issue(j + 1);
+                    // with tensor stores of o, the copy goes after MMA1 instead (the
+                    // previous chunk's o stores then have had time to read its buffer;
+                    // a part copied earlier shares the copy unit with them and lands later)
+                    if (!p.o_tma && j + 1 < total && ld_acquire(&R.ready[k * RING + (j + 1) % RING]) >= j + 2) {
+                        issue(j + 1, false);
                         issued_next = true;
                         KDA_TRACE_ANY(p, 17, j + 1);
                     }
@@ -1205,6 +1225,11 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
                     umma_f16(tmem + 128, umma_desc_sw128(a0 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
                              umma_desc_sw128(b0 + kk * 2048, 16384, 1024), idesc_qw, kk > 0);
                 umma_commit(bar_mma1);
+                if (p.o_tma && j + 1 < total && ld_acquire(&R.ready[k * RING + (j + 1) % RING]) >= j + 2) {
+                    issue(j + 1, false);
+                    issued_next = true;
+                    KDA_TRACE_ANY(p, 17, j + 1);
+                }
             }
 
             // (4) v_new = u - w S (TMEM lanes 64-127) -> fp16 [token][value] tile
@@ -1276,6 +1301,43 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
             wait_all(R, bar_mma23, j & 1, p.status);
             tc_fence_after();
             KDA_TRACE_EV(p, 16, j);
+            if (p.o_tma && nv == BT) {
+                // A full chunk of a plain o: staged in this chunk's slot buffer
+                // (every operand in it is consumed) as four 128-byte-swizzled
+                // [64][32] fp32 boxes, and written by four tensor stores that
+                // run while the next chunk starts (the next copy into this
+                // buffer waits for them to read it).
+                unsigned char *ob = smem + (b ? OFF_BUF1 : OFF_BUF0) + slice * (BT * 128);
+                if (quad < 2) {
+                    uint32_t r0[16], r1[16];
+                    tmem_ld16(tD, r0);
+                    tmem_ld16(tD + 16, r1);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int c4 = 0; c4 < 8; ++c4) {
+                        const uint32_t *r = c4 < 4 ? r0 + 4 * c4 : r1 + 4 * (c4 - 4);
+                        *reinterpret_cast<uint4 *>(ob + row * 128 + ((c4 ^ (row & 7)) << 4)) = make_uint4(r[0], r[1], r[2], r[3]);
+                    }
+                }
+                fence_proxy_async_shared();
+                tc_fence_before();
+                sync_compute();
+                if (tid == 0) {
+                    const unsigned char *o0 = smem + (b ? OFF_BUF1 : OFF_BUF0);
+#pragma unroll
+                    for (int s4 = 0; s4 < 4; ++s4) tma_store_3d(&p.tm_o, o0 + s4 * (BT * 128), 32 * s4, h, static_cast<int>(t0));
+                    bulk_commit();
+                }
+                KDA_TRACE_EV(p, 12, j);
+                if (tid == 0 && !issued_next && j + 1 < total) {
+                    if (wait_flag_geq(R, &R.ready[k * RING + (j + 1) % RING], j + 2, p.status)) {
+                        issue(j + 1, true);
+                        KDA_TRACE_ANY(p, 18, j + 1);
+                    } else
+                        misc[0] = 0;
+                }
+                continue;
+            }
             float *stg = reinterpret_cast<float *>(sS);  // [64][OST] fp32, spans the S16 and v_new tiles
             if (quad < 2) {
                 uint32_t r0[16], r1[16];
@@ -1330,7 +1392,7 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
             KDA_TRACE_EV(p, 12, j);
             if (tid == 0 && !issued_next && j + 1 < total) {
                 if (wait_flag_geq(R, &R.ready[k * RING + (j + 1) % RING], j + 2, p.status)) {
-                    issue(j + 1);
+                    issue(j + 1, false);
                     KDA_TRACE_ANY(p, 18, j + 1);
                 }
                 else
@@ -1355,6 +1417,7 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
         }
     }
     if (range_bad) set_status(p.status, KDA_ERR_VALUE_RANGE);
+    if (tid == 0) bulk_wait_all();  // the last o stores
     tc_fence_before();
     sync_compute();
     tc_fence_after();
@@ -1388,6 +1451,34 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_persistent_kernel(const __gri
 }
 
 // ------------------------------------------------------------------ host side
+// cuTensorMapEncodeTiled, looked up once through the runtime (no link to the driver library)
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+static EncodeTiledFn encode_tiled() {
+    static const EncodeTiledFn fn = [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return static_cast<EncodeTiledFn>(nullptr);
+        return reinterpret_cast<EncodeTiledFn>(f);
+    }();
+    return fn;
+}
+// map of o as [tokens][heads][128] fp32 with a box of 32 channels x 1 head x
+// 64 tokens and the 128-byte swizzle; false when the encoder is unavailable
+static bool encode_o(CUtensorMap *m, float *o, int64_t tokens, int heads) {
+    const EncodeTiledFn fn = encode_tiled();
+    if (!fn || tokens < 1) return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(DV), static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(tokens)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(DV) * 4, static_cast<cuuint64_t>(DV) * 4 * heads};
+    const cuuint32_t box[3] = {32u, 1u, static_cast<cuuint32_t>(BT)};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, o, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 static int num_sms() {
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -1463,6 +1554,8 @@ cudaError_t launch(Params p, size_t ws_bytes, cudaStream_t stream) {
     p.Cws = max_consumers(chains, grid);
     p.spin = p.debug ? SPIN_LIMIT_DEBUG : SPIN_LIMIT;
     if (ws_bytes < ring_offset(p.Cws) + static_cast<size_t>(p.Cws) * RING * SLOT_BYTES) return cudaErrorInvalidValue;
+    // a plain o leaves full chunks by tensor stores (else, and for partial chunks, by the warps)
+    p.o_tma = (p.o && !p.ngate && encode_o(&p.tm_o, p.o, p.Ttok, p.H)) ? 1 : 0;
     e = cudaMemsetAsync(p.ws, 0, ring_offset(p.C), stream);
     if (e != cudaSuccess) return e;
 #ifdef KDA_TRACE

@@ -1,5 +1,6 @@
 // Internal interface of the persistent producer/consumer kernel (not part of the C ABI).
 #pragma once
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
@@ -36,6 +37,11 @@ struct Params {
     const __nv_bfloat16 *ngate;  // [T][H][128] gate of the fused gated RMSNorm of o, or NULL (plain o)
     const float *nweight;        // [128] its per-channel weight
     float neps;                  // its epsilon
+    // set by launch: a tiled tensor map of o as [Ttok][H][128] fp32 (box 32
+    // channels x 1 head x 64 tokens, 128-byte swizzle), valid when o_tma is 1
+    // (a plain o: given, without the gated norm)
+    int32_t o_tma;
+    CUtensorMap tm_o;
 };
 
 // workspace: [64-byte header][ready C*RING][freed C*RING] padded to 1024, then the slots
