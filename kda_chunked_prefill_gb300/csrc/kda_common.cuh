@@ -42,6 +42,14 @@ __device__ __forceinline__ float2 unpack_f16(uint32_t u) {
 
 // Largest magnitude kept below fp16's finite limit (65504) with margin.
 constexpr float F16_SAFE = 60000.f;
+// Running maximum of magnitudes that turns NaN once any input is NaN
+// (max.NaN): one comparison of the result against F16_SAFE at the end then
+// flags both out-of-range and NaN values.
+__device__ __forceinline__ float max_abs_nan(float m, float x) {
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(m), "f"(fabsf(x)));
+    return r;
+}
 
 __device__ __forceinline__ float2 unpack_bf16(uint32_t u) {
     __nv_bfloat162 p = *reinterpret_cast<__nv_bfloat162 *>(&u);

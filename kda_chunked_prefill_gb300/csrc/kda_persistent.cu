@@ -407,7 +407,6 @@ __device__ __forceinline__ int g_elem(int r, int c) { return g_chunk(r, c & ~3) 
 // are free of bank conflicts and a group of 4 pairs stays 32 contiguous bytes
 __device__ __forceinline__ int qa_pair(int r, int c) { return r * 512 + ((((c >> 1) ^ ((r & 3) << 2))) << 3); }
 __device__ __forceinline__ int f_pair(int i, int j) { return i * (i - 1) / 2 + j; }
-__device__ __forceinline__ bool f16_ok(float x) { return fabsf(x) < F16_SAFE; }
 // The image leaves in two bulk stores: q_hat (rows 0-63 of A1) and kg as soon
 // as the elementwise step has written them, the rest after the solve.
 __device__ __forceinline__ void store_early(unsigned char *dst, const unsigned char *img) {
@@ -540,7 +539,7 @@ __device__ __forceinline__ void issue_loads(const Params &p, unsigned char *smem
 // Returns false when the slot wait gave up (timeout or abort).
 __device__ __forceinline__ bool run_task(const Params &p, const Ring &Rg, unsigned char *smem, const Task &cur,
                                          const int32_t *cu_s, int jmax, const Task &nxt, Task &nxt2, Cursor &cs, int &pending,
-                                         int pending_val, bool &gate_bad, bool &range_bad) {
+                                         int pending_val, bool &gate_bad, float &vmax) {
     unsigned char *img = smem + OFF_IMG;
     unsigned char *sQ = smem + OFF_Q, *sK = smem + OFF_K, *sV = smem + OFF_V;
     unsigned char *sGb = smem + OFF_GKB;  // G, swizzled (g_chunk / g_elem)
@@ -679,8 +678,10 @@ __device__ __forceinline__ bool run_task(const Params &p, const Ring &Rg, unsign
                 oQa[2 * q2] = tf32_rna(res[0][0]);
                 oQa[2 * q2 + 1] = tf32_rna(res[1][0]);
                 oKa[q2] = pack_bf16(res[0][1], res[1][1]);
-                range_bad |= !(f16_ok(res[0][2]) && f16_ok(res[1][2]) && f16_ok(res[0][3]) && f16_ok(res[1][3]) &&
-                               f16_ok(res[0][4]) && f16_ok(res[1][4]) && f16_ok(res[0][5]) && f16_ok(res[1][5]));
+#pragma unroll
+                for (int e = 0; e < 2; ++e)
+#pragma unroll
+                    for (int o = 2; o < 6; ++o) vmax = max_abs_nan(vmax, res[e][o]);
                 oBv[q2] = pack_f16(res[0][2], res[1][2]);
                 oBk[q2] = pack_f16(res[0][3], res[1][3]);
                 oQs[q2] = pack_f16(res[0][4], res[1][4]);
@@ -795,7 +796,7 @@ __device__ __forceinline__ bool run_task(const Params &p, const Ring &Rg, unsign
                     vq[e] = incl ? scale * aq[nt][2 * hf + e] : 0.f;
                     vk[e] = strict ? bt * ak[nt][2 * hf + e] : 0.f;
                     if (i == j) sLD[(i * 16 + tl) * 17 + sl + e] = vk[e];
-                    range_bad |= !(f16_ok(vq[e]) && f16_ok(vk[e]));
+                    vmax = max_abs_nan(max_abs_nan(vmax, vq[e]), vk[e]);
                 }
                 *reinterpret_cast<uint32_t *>(img + SL_AQK + tile_elem(64, t, s)) = pack_f16(vq[0], vq[1]);
                 *reinterpret_cast<uint32_t *>(sL + t * RSA + s) = pack_f16(vk[0], vk[1]);
@@ -825,7 +826,7 @@ __device__ __forceinline__ bool run_task(const Params &p, const Ring &Rg, unsign
             }
 #pragma unroll
             for (int r = 0; r < 16; ++r) {
-                range_bad |= !f16_ok(x[r]);
+                vmax = max_abs_nan(vmax, x[r]);
                 sT[(16 * i + r) * RSA + 16 * i + jc] = __float2half_rn(x[r]);
             }
         }
@@ -868,7 +869,7 @@ __device__ __forceinline__ bool run_task(const Params &p, const Ring &Rg, unsign
                 for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
                     for (int hf = 0; hf < 2; ++hf) {
-                        range_bad |= !(f16_ok(m[nt][2 * hf]) && f16_ok(m[nt][2 * hf + 1]));
+                        vmax = max_abs_nan(max_abs_nan(vmax, m[nt][2 * hf]), m[nt][2 * hf + 1]);
                         *reinterpret_cast<uint32_t *>(sT + (16 * i + gq + 8 * hf) * RSA + 16 * j + 8 * nt + 2 * qd) =
                             pack_f16(m[nt][2 * hf], m[nt][2 * hf + 1]);
                     }
@@ -886,7 +887,7 @@ __device__ __forceinline__ bool run_task(const Params &p, const Ring &Rg, unsign
                 for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
                     for (int hf = 0; hf < 2; ++hf) {
-                        range_bad |= !(f16_ok(t[nt][2 * hf]) && f16_ok(t[nt][2 * hf + 1]));
+                        vmax = max_abs_nan(max_abs_nan(vmax, t[nt][2 * hf]), t[nt][2 * hf + 1]);
                         *reinterpret_cast<uint32_t *>(sT + (16 * i + gq + 8 * hf) * RSA + 16 * j + 8 * nt + 2 * qd) =
                             pack_f16(-t[nt][2 * hf], -t[nt][2 * hf + 1]);
                     }
@@ -904,7 +905,7 @@ __device__ __forceinline__ bool run_task(const Params &p, const Ring &Rg, unsign
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
                     const int rr = 16 * xi + gq + 8 * hf, cc = col0 + 8 * nt + 2 * qd;
-                    range_bad |= !(f16_ok(acc[nt][2 * hf]) && f16_ok(acc[nt][2 * hf + 1]));
+                    vmax = max_abs_nan(max_abs_nan(vmax, acc[nt][2 * hf]), acc[nt][2 * hf + 1]);
                     *reinterpret_cast<uint32_t *>(img + uw_elem(isw, rr, cc)) = pack_f16(acc[nt][2 * hf], acc[nt][2 * hf + 1]);
                 }
             if (xi < 3) sync_compute();  // block diagonal d of T is complete
@@ -955,7 +956,8 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int pi
     Task nxt = get_task(misc + 10);
     sync_compute();
     if (cur.valid) issue_loads(p, smem, cur);
-    bool gate_bad = false, range_bad = false;
+    bool gate_bad = false;
+    float vmax = 0.f;  // largest magnitude packed into an fp16 operand (NaN if any was NaN)
     int pending = -1, pending_val = 0;  // REL_TID: the last slot stored but not yet published
     while (cur.valid) {
         KDA_TRACE_EV(p, 1, cur.j * p.C + cur.k);
@@ -963,7 +965,7 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int pi
         sync_compute();
         KDA_TRACE_EV(p, 20, 0);
         Task nxt2{0, 0, 0, 0, 0, 0, 0, 0};
-        if (!run_task(p, R, smem, cur, cu_s, jmax, nxt, nxt2, cs, pending, pending_val, gate_bad, range_bad))
+        if (!run_task(p, R, smem, cur, cu_s, jmax, nxt, nxt2, cs, pending, pending_val, gate_bad, vmax))
             break;
         if (tid == REL_TID) {
             pending = cur.k * RING + cur.j % RING;
@@ -982,7 +984,7 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int pi
     }
     cp_async_wait_all();
     if (gate_bad) set_status(p.status, KDA_ERR_GATE_RANGE);
-    if (range_bad) set_status(p.status, KDA_ERR_VALUE_RANGE);
+    if (!(vmax < F16_SAFE)) set_status(p.status, KDA_ERR_VALUE_RANGE);
 }
 }  // namespace prod
 
@@ -1009,7 +1011,6 @@ constexpr uint32_t TMEM_COLS = 256;
 constexpr int OST = 132;  // fp32 row stride of the o staging tile (64 x OST spans S16 + v_new); columns
                           // 128-131 hold the row's four slice sums of squares for the gated norm
 static_assert(64 * OST * 4 <= 32768 + 16384, "o staging fits in the state and v_new tiles");
-__device__ __forceinline__ bool f16_ok(float x) { return fabsf(x) < F16_SAFE; }
 
 // one 128-byte line of global memory towards L2 (no register result)
 __device__ __forceinline__ void prefetch_l2(const void *ptr) {
@@ -1108,7 +1109,8 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
     const uint32_t idesc_kv = umma_idesc_f16(true, true, 128, 128);   // kg^T x v_new
 
     int j = 0;
-    bool range_bad = false, alive = true;
+    bool alive = true;
+    float vmax = 0.f;  // largest magnitude packed into an fp16 operand (NaN if any was NaN)
     const int nchains = sched_count(p, smem, k);
     for (int r = 0; r < nchains && alive; ++r) {
         const int ch = sched_chain(p, smem, k, r);
@@ -1196,7 +1198,7 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
                         const float x0 = __uint_as_float(r[2 * e]), x1 = __uint_as_float(r[2 * e + 1]);
-                        range_bad |= !(f16_ok(x0) && f16_ok(x1));
+                        vmax = max_abs_nan(max_abs_nan(vmax, x0), x1);
                         hp[e] = pack_f16(x0, x1);
                     }
                     const int c8 = 32 * slice + 16 * cb;
@@ -1254,7 +1256,7 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
                             const float2 u2 = unpack_f16(uw[e]);
                             const float y0 = u2.x - __uint_as_float(r[8 * hh + 2 * e]);
                             const float y1 = u2.y - __uint_as_float(r[8 * hh + 2 * e + 1]);
-                            range_bad |= !(f16_ok(y0) && f16_ok(y1));
+                            vmax = max_abs_nan(max_abs_nan(vmax, y0), y1);
                             vp[e] = pack_f16(y0, y1);
                         }
                         *reinterpret_cast<uint4 *>(sVN + tile_chunk(64, t, c8 + 8 * hh)) = make_uint4(vp[0], vp[1], vp[2], vp[3]);
@@ -1416,7 +1418,7 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
             }
         }
     }
-    if (range_bad) set_status(p.status, KDA_ERR_VALUE_RANGE);
+    if (!(vmax < F16_SAFE)) set_status(p.status, KDA_ERR_VALUE_RANGE);
     if (tid == 0) bulk_wait_all();  // the last o stores
     tc_fence_before();
     sync_compute();
