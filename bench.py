@@ -13,7 +13,8 @@ independent, so there is no collective on the data path).
 
 Extra keys: ``roofline`` (HBM-bound: algorithmic bytes per launch / mean
 launch time, against the measured copy bandwidth), ``e2e`` (the same metric
-through the C ABI with pinned host buffers, copies inside the timed region),
+through the C ABI with pinned host buffers, every host-device transfer inside
+the timed region),
 ``cpu_baseline`` (the fp64 oracle on the host cores, a bounded sample of the
 same workload), ``clocks`` (nvidia-smi samples during the timed region) and
 ``gpu_launches`` (kernels this library launched in the timed region).
@@ -367,7 +368,7 @@ def bench_gpu(a, world, rank, local):
     ms_per_step = 1e3 * total_s / a.steps
     value = T * a.steps * world / total_s
 
-    # e2e through the C ABI with pinned host buffers (copies inside the timed region)
+    # e2e through the C ABI with pinned host buffers (every transfer inside the timed region)
     host = {key: (None if inp[key] is None else inp[key].pin_memory()) for key in
             ("q", "k", "v", "g", "beta", "cu_seqlens", "initial_state") + (("norm_gate",) if a.gated_norm else ())}
     o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
@@ -378,8 +379,8 @@ def bench_gpu(a, world, rank, local):
 
     plain_prefill = not (decode or a.split or a.gated_norm or a.raw_gates)
     if plain_prefill:
-        # kda_chunk_fwd_host: the same call on the pinned host buffers, each
-        # group's copies overlapped with its neighbours' computation
+        # kda_chunk_fwd_host: the same call on the pinned host buffers, which
+        # the kernel reads and writes in place
         hbuf = torch.empty(kda.host_buffer_size(inp["cu_seqlens"], H, inp["initial_state"] is not None, True),
                            dtype=torch.uint8, device=dev)
         s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
@@ -450,8 +451,9 @@ def bench_gpu(a, world, rank, local):
                         "p90": sorted(step_ms)[(9 * len(step_ms)) // 10]},
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "steps": e2e_steps,
-                    "call": ("kda_chunk_fwd_host (pinned host buffers, copies overlapped per group of sequences)"
-                             if plain_prefill else "host-to-device copies, the call, device-to-host copies")},
+                    "call": ("kda_chunk_fwd_host on pinned host buffers (one launch reads the inputs and writes "
+                             "o and final_state in host memory over the CPU-GPU link; the byte counts are what "
+                             "crosses it)" if plain_prefill else "host-to-device copies, the call, device-to-host copies")},
             "gpu_launches": a.steps * (1 if decode else (5 if split_L > 0 else kda.chunk_fwd_launches(N, T, H))),
             "clocks": clocks,
             "cpu_baseline": cpu,

@@ -248,9 +248,15 @@ size_t kda_chunk_fwd_split_workspace_size(const int32_t *cu_seqlens_host, int32_
                                           int32_t segment_chunks);
 
 /*
- * kda_chunk_fwd_host — kda_chunk_fwd on inputs and outputs in HOST memory, with
- * the transfers overlapped with the computation (a deployment convenience of
- * this library; the pages have no counterpart). The sequences are cut into
+ * kda_chunk_fwd_host — kda_chunk_fwd on inputs and outputs in HOST memory (a
+ * deployment convenience of this library; the pages have no counterpart).
+ * With groups = 0 and every buffer in page-locked host memory that the device
+ * addresses at the same pointer (cudaHostAlloc memory, or cudaHostRegister'ed
+ * memory mapped into the device's address space, under unified addressing),
+ * one kernel launch reads the inputs and writes o and final_state in host
+ * memory directly over the CPU-GPU link, with no staging copy; h2d_stream and
+ * d2h_stream are then unused. Otherwise the transfers are overlapped with the
+ * computation: the sequences are cut into
  * `groups` groups of whole sequences with about equal token counts (0: 4;
  * at most 16 and num_seqs). Group i's q, k, v, g, beta and initial states are
  * copied to the device on h2d_stream; `stream` waits for them and runs the

@@ -355,9 +355,11 @@ def kda_chunk_fwd_host(q, k, v, g, beta, cu_seqlens_host, initial_state, scale: 
                        final_state, device_buffer, status=None, groups: int = 0, stream=None, h2d_stream=None,
                        d2h_stream=None) -> int:
     """Call ``kda_chunk_fwd_host``: q .. beta, initial_state, o and final_state
-    are CPU tensors (page-locked for overlap; layouts as ``kda_chunk_fwd``),
-    ``device_buffer`` a CUDA uint8 tensor of ``host_buffer_size(...)`` bytes.
-    The results are in ``o`` / ``final_state`` once ``stream`` is synchronised."""
+    are CPU tensors (layouts as ``kda_chunk_fwd``), ``device_buffer`` a CUDA uint8
+    tensor of ``host_buffer_size(...)`` bytes. With ``groups=0`` and page-locked
+    tensors (``pin_memory()``) the kernel reads and writes them in place; else
+    the copies of groups of sequences overlap the computation. The results are
+    in ``o`` / ``final_state`` once ``stream`` is synchronised."""
     T, H, D = q.shape
     cu, cu_ptr = _host_cu(cu_seqlens_host)
     N = cu.numel() - 1

@@ -1,5 +1,12 @@
 // kda_chunk_fwd_host: the chunked-prefill forward on inputs and outputs in host
-// memory, with the transfers overlapped with the computation.
+// memory.
+//
+// When every buffer is page-locked host memory that the device addresses in
+// place (cudaHostAlloc memory, or cudaHostRegister'ed memory mapped, under
+// unified addressing) and the caller lets the library choose the grouping,
+// one launch of the chunked kernel reads the inputs and writes o and the
+// final states in host memory directly over the CPU-GPU link: no staging
+// copies at all. Otherwise the transfers are overlapped with the computation:
 //
 // The batch is cut into groups of whole sequences of about equal token counts.
 // Group i's inputs go to the device on the H2D stream; the compute stream waits
@@ -63,10 +70,22 @@ Layout layout_for(const int32_t *cu, int N, int H, bool with_init, bool with_fin
     l.o = take(T * H * DV * 4);
     l.fs = take(with_final ? static_cast<size_t>(N) * H * STATE * 4 : 0);
     l.cu = take(static_cast<size_t>(N + static_cast<int>(first.size())) * 4);
-    const size_t ring = pers::workspace_bytes(max_chains);
+    // the in-place form runs all N x H chains in one launch
+    const size_t ring = pers::workspace_bytes(std::max<int64_t>(max_chains, static_cast<int64_t>(N) * H));
     l.ring = take(ring);
     l.total = ring == 0 ? 0 : at;
     return l;
+}
+
+// true for NULL and for page-locked host memory the device addresses at the same pointer
+bool addressable_in_place(const void *p) {
+    if (!p) return true;
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return false;
+    }
+    return a.type == cudaMemoryTypeHost && a.devicePointer == p;
 }
 
 int groups_for(int N, int32_t groups) {
@@ -121,9 +140,38 @@ kda_status_t kda_chunk_fwd_host(const void *q, const void *k, const void *v, con
     }
 
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    unsigned char *buf = static_cast<unsigned char *>(device_buffer);
+    if (groups == 0 && total_tokens > 0 && addressable_in_place(q) && addressable_in_place(k) &&
+        addressable_in_place(v) && addressable_in_place(g) && addressable_in_place(beta) &&
+        addressable_in_place(initial_state) && addressable_in_place(o) && addressable_in_place(final_state)) {
+        // in place: one launch on the host buffers (only the offsets and the ring are in device memory)
+        bool ok = !status_dev || cudaMemsetAsync(status_dev, 0, sizeof(int32_t), cs) == cudaSuccess;
+        // pageable source: staged before the call returns
+        ok = ok && cudaMemcpyAsync(buf + l.cu, cu_seqlens_host, static_cast<size_t>(N + 1) * 4, cudaMemcpyHostToDevice,
+                                   cs) == cudaSuccess;
+        if (!ok) return KDA_ERR_CUDA;
+        kda::pers::Params p{};
+        p.q = static_cast<const __nv_bfloat16 *>(q);
+        p.k = static_cast<const __nv_bfloat16 *>(k);
+        p.v = static_cast<const __nv_bfloat16 *>(v);
+        p.g = g;
+        p.beta = beta;
+        p.cu = reinterpret_cast<const int32_t *>(buf + l.cu);
+        p.N = N;
+        p.T = total_tokens;
+        p.Ttok = total_tokens;
+        p.H = H;
+        p.s0 = initial_state;
+        p.scale = scale;
+        p.lb = lower_bound;
+        p.o = o;
+        p.sT = final_state;
+        p.status = status_dev;
+        p.ws = buf + l.ring;
+        return kda::pers::launch(p, l.total - l.ring, cs) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+    }
     cudaStream_t in = h2d_stream ? reinterpret_cast<cudaStream_t>(h2d_stream) : cs;
     cudaStream_t out = d2h_stream ? reinterpret_cast<cudaStream_t>(d2h_stream) : cs;
-    unsigned char *buf = static_cast<unsigned char *>(device_buffer);
     std::vector<cudaEvent_t> ev(2 * G + 2, nullptr);
     auto release = [&]() {
         for (cudaEvent_t e : ev)

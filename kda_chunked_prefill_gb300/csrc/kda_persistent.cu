@@ -1556,8 +1556,15 @@ cudaError_t launch(Params p, size_t ws_bytes, cudaStream_t stream) {
     p.Cws = max_consumers(chains, grid);
     p.spin = p.debug ? SPIN_LIMIT_DEBUG : SPIN_LIMIT;
     if (ws_bytes < ring_offset(p.Cws) + static_cast<size_t>(p.Cws) * RING * SLOT_BYTES) return cudaErrorInvalidValue;
-    // a plain o leaves full chunks by tensor stores (else, and for partial chunks, by the warps)
-    p.o_tma = (p.o && !p.ngate && encode_o(&p.tm_o, p.o, p.Ttok, p.H)) ? 1 : 0;
+    // a plain o in device memory leaves full chunks by tensor stores (else, and
+    // for partial chunks, by the warps: an o in mapped host memory, for one)
+    bool o_device = false;
+    if (p.o) {
+        cudaPointerAttributes at{};
+        o_device = cudaPointerGetAttributes(&at, p.o) == cudaSuccess && at.type == cudaMemoryTypeDevice;
+        (void)cudaGetLastError();  // clear a failed query
+    }
+    p.o_tma = (o_device && !p.ngate && encode_o(&p.tm_o, p.o, p.Ttok, p.H)) ? 1 : 0;
     e = cudaMemsetAsync(p.ws, 0, ring_offset(p.C), stream);
     if (e != cudaSuccess) return e;
 #ifdef KDA_TRACE

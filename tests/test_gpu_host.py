@@ -1,8 +1,10 @@
-"""kda_chunk_fwd_host: the forward on host-resident inputs and outputs, with the
-copies of each group of sequences overlapped with the computation of its
-neighbours. The kernel's arithmetic per (sequence, head) chain does not depend
-on which other chains share the launch, so every grouping must reproduce the
-device call bit for bit."""
+"""kda_chunk_fwd_host: the forward on host-resident inputs and outputs. With the
+default grouping and page-locked buffers the device addresses in place, one
+launch reads and writes the host buffers directly; with an explicit grouping
+(or pageable memory) the copies of each group of sequences overlap the
+computation of its neighbours. The kernel's arithmetic per (sequence, head)
+chain does not depend on which other chains share the launch or where the
+buffers live, so every form must reproduce the device call bit for bit."""
 import pytest
 import torch
 
@@ -68,3 +70,12 @@ def test_host_call_with_pageable_memory_and_no_final_state():
     o_d, _ = pu.run_gpu(inp)
     o_h, fs_h = _host_call(inp, 2, pinned=False, with_final=False)
     assert fs_h is None and torch.equal(o_h, o_d.cpu())
+
+
+def test_host_call_in_place_with_empty_sequences_and_aliasing():
+    """The in-place form (default grouping, pinned buffers): empty sequences pass
+    their states through and the final states overwrite the initial ones."""
+    inp = kin.make_inputs([0, 0, 150, 0, 64], 2, seed=34, state_std=0.02)
+    o_d, fs_d = pu.run_gpu(inp)
+    o_h, fs_h = _host_call(inp, 0, alias=True)
+    assert torch.equal(o_h, o_d.cpu()) and torch.equal(fs_h, fs_d.cpu())
