@@ -616,63 +616,52 @@ __device__ __forceinline__ bool run_task(const Params &p, const Ring &Rg, unsign
     // ---- steps 2a/4a: elementwise operands; q_hat, kg, beta*v and
     // beta*k*e^G go straight into the slot image
     {
-        // thread: channels c8..c8+7 of rows r0 and r0 + 8, both in sub-block i
-        const int ew_i = tid >> 7, ew_c8 = (tid & 15) << 3, ew_r0 = 16 * ew_i + ((tid >> 4) & 7);
-        float Gv[2][8];
-        uint4 qv[2], kv[2], vv[2];
+        // warp w: rows 4w .. 4w+3 (all in sub-block w / 4); lane: channels
+        // 4 lane .. 4 lane + 3, so that every fp32 access of a warp is one
+        // contiguous 512-byte row and every 16-bit one a 256-byte row
+        const int ew_i = warp >> 2, c4 = lane << 2, r0 = warp << 2;
+        const int h8 = (c4 & 4) << 1;  // byte offset of these 4 channels in their 16-byte chunk
+        float4 Gv[4];
+        uint2 qv[4], kv[4], vv[4];
 #pragma unroll
-        for (int it = 0; it < 2; ++it) {
-            const int r = ew_r0 + 8 * it, c8 = ew_c8;
-            const float4 a = *reinterpret_cast<const float4 *>(sGb + g_chunk(r, c8));
-            const float4 b = *reinterpret_cast<const float4 *>(sGb + g_chunk(r, c8 + 4));
-            Gv[it][0] = a.x; Gv[it][1] = a.y; Gv[it][2] = a.z; Gv[it][3] = a.w;
-            Gv[it][4] = b.x; Gv[it][5] = b.y; Gv[it][6] = b.z; Gv[it][7] = b.w;
-            const int tc = tile_chunk(64, r, c8);
-            qv[it] = *reinterpret_cast<const uint4 *>(sQ + tc);
-            kv[it] = *reinterpret_cast<const uint4 *>(sK + tc);
-            vv[it] = *reinterpret_cast<const uint4 *>(sV + tc);
+        for (int it = 0; it < 4; ++it) {
+            const int r = r0 + it;
+            Gv[it] = *reinterpret_cast<const float4 *>(sGb + g_chunk(r, c4));
+            const int tc = tile_chunk(64, r, c4 & ~7) + h8;
+            qv[it] = *reinterpret_cast<const uint2 *>(sQ + tc);
+            kv[it] = *reinterpret_cast<const uint2 *>(sK + tc);
+            vv[it] = *reinterpret_cast<const uint2 *>(sV + tc);
         }
         sync_compute();  // G and q are read: kb and q*a overwrite them below
-        float GM[8], EM[8], EL[8];
-        {
-            const int i = ew_i, c8 = ew_c8;
-            const float4 a0 = *reinterpret_cast<const float4 *>(sTab + TGM + i * 128 + c8);
-            const float4 a1 = *reinterpret_cast<const float4 *>(sTab + TGM + i * 128 + c8 + 4);
-            const float4 b0 = *reinterpret_cast<const float4 *>(sTab + TEM + i * 128 + c8);
-            const float4 b1 = *reinterpret_cast<const float4 *>(sTab + TEM + i * 128 + c8 + 4);
-            const float4 d0 = *reinterpret_cast<const float4 *>(sTab + TEL + i * 128 + c8);
-            const float4 d1 = *reinterpret_cast<const float4 *>(sTab + TEL + i * 128 + c8 + 4);
-            GM[0] = a0.x; GM[1] = a0.y; GM[2] = a0.z; GM[3] = a0.w; GM[4] = a1.x; GM[5] = a1.y; GM[6] = a1.z; GM[7] = a1.w;
-            EM[0] = b0.x; EM[1] = b0.y; EM[2] = b0.z; EM[3] = b0.w; EM[4] = b1.x; EM[5] = b1.y; EM[6] = b1.z; EM[7] = b1.w;
-            EL[0] = d0.x; EL[1] = d0.y; EL[2] = d0.z; EL[3] = d0.w; EL[4] = d1.x; EL[5] = d1.y; EL[6] = d1.z; EL[7] = d1.w;
-        }
+        const float4 GM = *reinterpret_cast<const float4 *>(sTab + TGM + ew_i * 128 + c4);
+        const float4 EM = *reinterpret_cast<const float4 *>(sTab + TEM + ew_i * 128 + c4);
+        const float4 EL = *reinterpret_cast<const float4 *>(sTab + TEL + ew_i * 128 + c4);
+        const float gm[4] = {GM.x, GM.y, GM.z, GM.w}, em[4] = {EM.x, EM.y, EM.z, EM.w}, el[4] = {EL.x, EL.y, EL.z, EL.w};
 #pragma unroll
-        for (int it = 0; it < 2; ++it) {
-            const int r = ew_r0 + 8 * it, c8 = ew_c8;
+        for (int it = 0; it < 4; ++it) {
+            const int r = r0 + it;
             const float bt = sBeta[r];
-            const int tc = tile_chunk(64, r, c8);
-            const uint32_t *qw = reinterpret_cast<const uint32_t *>(&qv[it]);
-            const uint32_t *kw = reinterpret_cast<const uint32_t *>(&kv[it]);
-            const uint32_t *vw = reinterpret_cast<const uint32_t *>(&vv[it]);
-            uint32_t oQa[8], oKa[4], oBv[4], oBk[4], oQs[4], oKg[4];
-            float kb[8];
+            const float gv[4] = {Gv[it].x, Gv[it].y, Gv[it].z, Gv[it].w};
+            const uint32_t qw[2] = {qv[it].x, qv[it].y}, kw[2] = {kv[it].x, kv[it].y}, vw[2] = {vv[it].x, vv[it].y};
+            uint32_t oQa[4], oKa[2], oBv[2], oBk[2], oQs[2], oKg[2];
+            float kb[4];
 #pragma unroll
-            for (int q2 = 0; q2 < 4; ++q2) {
+            for (int q2 = 0; q2 < 2; ++q2) {
                 const float2 qf = unpack_bf16(qw[q2]), kf = unpack_bf16(kw[q2]), vf = unpack_bf16(vw[q2]);
                 float res[2][6];
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const int ce = 2 * q2 + e;
                     const float qq = e ? qf.y : qf.x, kk = e ? kf.y : kf.x, vv2 = e ? vf.y : vf.x;
-                    const float x = Gv[it][ce] - GM[ce];
+                    const float x = gv[ce] - gm[ce];
                     const float a = ex2(x), b = ex2(-x);
-                    const float eG = a * EM[ce];
+                    const float eG = a * em[ce];
                     res[e][0] = qq * a;            // q e^(G - G_m)
                     res[e][1] = kk * a;            // k e^(G - G_m)
                     res[e][2] = bt * vv2;          // beta v
                     res[e][3] = bt * kk * eG;      // beta k e^G
                     res[e][4] = scale * qq * eG;   // scale q e^G
-                    res[e][5] = kk * b * EL[ce];   // k e^(G_last - G)
+                    res[e][5] = kk * b * el[ce];   // k e^(G_last - G)
                     kb[ce] = kk * b;               // k e^(G_m - G)
                 }
                 oQa[2 * q2] = tf32_rna(res[0][0]);
@@ -687,15 +676,14 @@ __device__ __forceinline__ bool run_task(const Params &p, const Ring &Rg, unsign
                 oQs[q2] = pack_f16(res[0][4], res[1][4]);
                 oKg[q2] = pack_f16(res[0][5], res[1][5]);
             }
-            *reinterpret_cast<uint4 *>(sQ + qa_pair(r, c8)) = make_uint4(oQa[0], oQa[1], oQa[2], oQa[3]);
-            *reinterpret_cast<uint4 *>(sQ + qa_pair(r, c8) + 16) = make_uint4(oQa[4], oQa[5], oQa[6], oQa[7]);
-            *reinterpret_cast<uint4 *>(sK + tc) = *reinterpret_cast<uint4 *>(oKa);
-            *reinterpret_cast<float4 *>(sKB + r * RSF + c8) = make_float4(kb[0], kb[1], kb[2], kb[3]);
-            *reinterpret_cast<float4 *>(sKB + r * RSF + c8 + 4) = make_float4(kb[4], kb[5], kb[6], kb[7]);
-            *reinterpret_cast<uint4 *>(img + uw_chunk(false, r, c8)) = *reinterpret_cast<uint4 *>(oBv);
-            *reinterpret_cast<uint4 *>(img + uw_chunk(true, r, c8)) = *reinterpret_cast<uint4 *>(oBk);
-            *reinterpret_cast<uint4 *>(img + SL_A1 + tile_chunk(128, r, c8)) = *reinterpret_cast<uint4 *>(oQs);
-            *reinterpret_cast<uint4 *>(img + SL_KG + tile_chunk(64, r, c8)) = *reinterpret_cast<uint4 *>(oKg);
+            const int tc = tile_chunk(64, r, c4 & ~7) + h8;
+            *reinterpret_cast<uint4 *>(sQ + qa_pair(r, c4)) = make_uint4(oQa[0], oQa[1], oQa[2], oQa[3]);
+            *reinterpret_cast<uint2 *>(sK + tc) = make_uint2(oKa[0], oKa[1]);
+            *reinterpret_cast<float4 *>(sKB + r * RSF + c4) = make_float4(kb[0], kb[1], kb[2], kb[3]);
+            *reinterpret_cast<uint2 *>(img + uw_chunk(false, r, c4 & ~7) + h8) = make_uint2(oBv[0], oBv[1]);
+            *reinterpret_cast<uint2 *>(img + uw_chunk(true, r, c4 & ~7) + h8) = make_uint2(oBk[0], oBk[1]);
+            *reinterpret_cast<uint2 *>(img + SL_A1 + tile_chunk(128, r, c4 & ~7) + h8) = make_uint2(oQs[0], oQs[1]);
+            *reinterpret_cast<uint2 *>(img + SL_KG + tile_chunk(64, r, c4 & ~7) + h8) = make_uint2(oKg[0], oKg[1]);
         }
         if (tid < 32)
             *reinterpret_cast<float4 *>(img + SL_D + 16 * tid) = *reinterpret_cast<const float4 *>(sTab + TD + 4 * tid);
