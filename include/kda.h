@@ -301,7 +301,7 @@ size_t kda_chunk_fwd_workspace_size(int32_t num_seqs, int32_t num_heads);
 /* Size of the fixed device scratch array behind kda_chunk_fwd_static_scratch
  * (a build may define a different size). */
 #ifndef KDA_STATIC_SCRATCH_BYTES
-#define KDA_STATIC_SCRATCH_BYTES (24u << 20)
+#define KDA_STATIC_SCRATCH_BYTES (26u << 20)
 #endif
 
 /*
@@ -314,7 +314,7 @@ size_t kda_chunk_fwd_workspace_size(int32_t num_seqs, int32_t num_heads);
  *
  * Arguments, layouts, results and asynchronous behaviour are those of
  * kda_chunk_fwd, without the workspace pair. The scratch instead comes from
- * one fixed __device__ array of KDA_STATIC_SCRATCH_BYTES (24 MiB) compiled into
+ * one fixed __device__ array of KDA_STATIC_SCRATCH_BYTES (26 MiB) compiled into
  * the library, which every GPU that loads the library holds until the process
  * exits. No call allocates or frees memory.
  *
@@ -351,12 +351,27 @@ kda_status_t kda_chunk_fwd_static_scratch(const void *q, const void *k, const vo
  *                             (after its own copies have landed and its tensor
  *                             memory is freed) and the context stays usable.
  *
- * With any flag set, a wait gives up after 2^14 polls (milliseconds) instead
- * of 2^24; o and final_state are then unspecified. debug_flags = 0 is exactly
- * kda_chunk_fwd. Unknown flags return KDA_ERR_INVALID_ARG.
+ *   KDA_DEBUG_WY_PRODUCER     the producer CTAs form the WY product
+ *                             X = T [beta v | beta k e^G] (u and w go to the
+ *                             consumers), whatever the launch's own choice.
+ *   KDA_DEBUG_WY_CONSUMER     the consumer CTAs form it (they receive T, beta v
+ *                             and beta k e^G and compute v_new = T (beta v -
+ *                             beta k e^G S)). Both forms compute the same o and
+ *                             final_state within the parity bar; a launch
+ *                             normally picks one from the batch's shape (the
+ *                             consumers' form only where all sequences can be
+ *                             of one length and the consumers have slack).
+ *                             Setting both returns KDA_ERR_INVALID_ARG.
+ *
+ * With KDA_DEBUG_WITHHOLD_READY set, a wait gives up after 2^14 polls
+ * (milliseconds) instead of 2^24; o and final_state are then unspecified.
+ * debug_flags = 0 is exactly kda_chunk_fwd. Unknown flags return
+ * KDA_ERR_INVALID_ARG.
  * (Not part of the method: the pages define no counterpart.)
  */
 #define KDA_DEBUG_WITHHOLD_READY 1u
+#define KDA_DEBUG_WY_PRODUCER 2u
+#define KDA_DEBUG_WY_CONSUMER 4u
 kda_status_t kda_chunk_fwd_debug(const void *q, const void *k, const void *v, const float *g,
                                  const float *beta, const int32_t *cu_seqlens, int32_t num_seqs,
                                  int64_t total_tokens, int32_t num_heads, int32_t head_dim_k,

@@ -27,6 +27,8 @@ KDA_ERR_VALUE_RANGE = 7
 KDA_ERR_SCRATCH_TOO_SMALL = 8
 KDA_ERR_BOUNDS = 9
 KDA_DEBUG_WITHHOLD_READY = 1
+KDA_DEBUG_WY_PRODUCER = 2  # the producer CTAs form the WY product
+KDA_DEBUG_WY_CONSUMER = 4  # the consumer CTAs form it
 
 HEAD_DIM = 128
 EXPORTED = ("kda_chunk_fwd", "kda_chunk_fwd_workspace_size", "kda_chunk_fwd_static_scratch",

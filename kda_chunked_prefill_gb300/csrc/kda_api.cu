@@ -134,7 +134,9 @@ kda_status_t kda_chunk_fwd_debug(const void *q, const void *k, const void *v, co
                                  float lower_bound, float *o, float *final_state,
                                  int32_t *status_dev, void *workspace, size_t workspace_bytes,
                                  kda_stream_t stream, uint32_t debug_flags) {
-    if (debug_flags & ~static_cast<uint32_t>(KDA_DEBUG_WITHHOLD_READY)) return KDA_ERR_INVALID_ARG;
+    constexpr uint32_t known = KDA_DEBUG_WITHHOLD_READY | KDA_DEBUG_WY_PRODUCER | KDA_DEBUG_WY_CONSUMER;
+    if ((debug_flags & ~known) || ((debug_flags & KDA_DEBUG_WY_PRODUCER) && (debug_flags & KDA_DEBUG_WY_CONSUMER)))
+        return KDA_ERR_INVALID_ARG;
     Extras x;
     x.debug = debug_flags;
     return fwd_impl(q, k, v, g, beta, cu_seqlens, num_seqs, total_tokens, num_heads, head_dim_k, head_dim_v,

@@ -21,6 +21,7 @@
 // All waits are bounded: a wait that runs out sets KDA_ERR_TIMEOUT and an abort
 // word in the workspace, and every CTA then returns.
 
+#include <cmath>
 #include "kda.h"
 #include "kda_common.cuh"
 #include "kda_persistent.h"
@@ -32,7 +33,7 @@ constexpr int NCOMP = 512;            // 16 warps, all computing (<= 128 registe
 constexpr int NTHREADS = NCOMP;
 constexpr int NWARPS = NCOMP / 32;
 constexpr long long SPIN_LIMIT = 1ll << 24;         // polls before a wait gives up (normal calls)
-constexpr long long SPIN_LIMIT_DEBUG = 1ll << 14;   // the same under any KDA_DEBUG_* flag
+constexpr long long SPIN_LIMIT_DEBUG = 1ll << 14;   // the same under KDA_DEBUG_WITHHOLD_READY
 #ifdef KDA_TRACE
 constexpr int TRACE_COUNTS_OFFSET = 231424;  // past every role's tiles (checked below), 16 ints
 #endif
@@ -44,11 +45,16 @@ constexpr int TRACE_COUNTS_OFFSET = 231424;  // past every role's tiles (checked
 //   U   u            fp16, [token][value] (64 x 128)
 //   D   e^(G_last)   fp32, 128
 //   AQK scale * Aqk  fp16, [t][s] (64 x 64), causal incl. diagonal
+//   T   T = (I + L)^-1 fp16, [t][s] (64 x 64), lower block triangle: only in
+//       the launches where the consumers form the WY product (then A1's rows
+//       64-127 hold beta k e^G and U holds beta v instead of w and u), whose
+//       ring slots are SLOT_BYTES apart; otherwise slots are SL_T apart
 // 128-byte swizzle: row r of a 128-byte-wide atom column keeps its 16-byte
 // chunk c at position c ^ (r mod 8); wider tiles are split into 64-element
 // atom columns stored one after the other.
-constexpr int SL_A1 = 0, SL_KG = 32768, SL_U = 49152, SL_D = 65536, SL_AQK = 66560;
-static_assert(SLOT_BYTES == 74752, "slot size");
+constexpr int SL_A1 = 0, SL_KG = 32768, SL_U = 49152, SL_D = 65536, SL_AQK = 66560, SL_T = 74752;
+static_assert(SLOT_BYTES == SL_T + 8192, "slot size");
+template <bool WY> constexpr int SLOT_STRIDE = WY ? SLOT_BYTES : SL_T;  // WY: the consumers form the WY product
 
 __device__ __forceinline__ int swz(int r, int chunk) { return (chunk ^ (r & 7)) << 4; }
 // byte offset of the 16-byte chunk holding columns [c8, c8+8) of row r of a
@@ -373,8 +379,8 @@ namespace prod {
 constexpr int RSF = 136, RSA = 72;
 constexpr int SZ_T = BT * DK * 2;             // 16384
 constexpr int SZ_F = BT * RSF * 4;            // 34816 (kb keeps a padded row stride)
-constexpr int OFF_IMG = 0;                    // slot image: the bytes of one ring slot
-constexpr int OFF_Q = OFF_IMG + SLOT_BYTES;   // q; then q*a as tf32 (fp32 [64][128], spans OFF_Q and OFF_QLO)
+constexpr int OFF_IMG = 0;                    // slot image: a ring slot up to T (T has its own tile, OFF_T)
+constexpr int OFF_Q = OFF_IMG + SL_T;         // q; then q*a as tf32 (fp32 [64][128], spans OFF_Q and OFF_QLO)
 constexpr int OFF_QLO = OFF_Q + SZ_T;
 constexpr int OFF_K = OFF_QLO + SZ_T;         // k -> k*a (bf16)
 constexpr int OFF_V = OFF_K + SZ_T;           // v (bf16)
@@ -382,7 +388,8 @@ constexpr int OFF_GKB = OFF_V + SZ_T;         // g -> G (fp32, swizzled), then k
 constexpr int SZ_A = BT * RSA * 2;            // 9216
 constexpr int OFF_L = OFF_GKB + SZ_F;         // L (fp16 [64][RSA])
 constexpr int OFF_LD = OFF_L + SZ_A;          // diagonal blocks of L, fp32 [4][16][17]
-constexpr int OFF_T = OFF_LD + 4352;          // T = (I+L)^-1, fp16 [64][RSA] (lower blocks)
+constexpr int OFF_T = OFF_LD + 4352;          // T = (I+L)^-1, fp16 [64][RSA] (lower blocks); with WY
+                                              // the swizzled [64][64] tile the consumer reads
 constexpr int OFF_TAB = OFF_T + SZ_A;         // per-channel tables, fp32 [20][128]
 constexpr int OFF_BETA = OFF_TAB + 10240;
 constexpr int OFF_MISC = OFF_BETA + 256;      // flags and the task broadcast (32 ints)
@@ -393,6 +400,7 @@ static_assert(OFF_GPAR % 16 == 0, "cp.async destinations are 16-byte aligned");
 // ten tiles (three on partitions 0 and 1, two on 2 and 3); the diagonal
 // inverses run on warps 10, 11, 14, 15 (partitions 2 and 3) and the ring work,
 // mostly waiting, on warps 12 and 13 (partitions 0 and 1).
+constexpr int BAR_TB = 6;                     // WY: named barrier of warps 0-2 building T's block diagonals
 constexpr int SYNC_TID = 13 * 32;             // lane 0 of warp 13: draws tasks
 constexpr int REL_TID = 12 * 32;              // lane 0 of warp 12: waits for free slots, stores and publishes images
 constexpr int TGM = 0, TGL = 4 * 128, TEM = 5 * 128, TEL = 9 * 128, TF = 13 * 128, TD = 19 * 128;
@@ -416,10 +424,13 @@ __device__ __forceinline__ void store_early(unsigned char *dst, const unsigned c
     bulk_s2g(dst + SL_KG, img + SL_KG, SL_U - SL_KG);          // kg
     bulk_commit();
 }
+// (With WY, w and u are beta k e^G and beta v, and T follows from its own tile.)
+template <bool WY>
 __device__ __forceinline__ void store_late(unsigned char *dst, const unsigned char *img) {
     bulk_s2g(dst + SL_A1 + 8192, img + SL_A1 + 8192, 8192);    // w, channels 0-63
     bulk_s2g(dst + SL_A1 + 24576, img + SL_A1 + 24576, 8192);  // w, channels 64-127
-    bulk_s2g(dst + SL_U, img + SL_U, SLOT_BYTES - SL_U);       // u, e^(G_last), scale*Aqk
+    bulk_s2g(dst + SL_U, img + SL_U, SL_T - SL_U);             // u, e^(G_last), scale*Aqk
+    if constexpr (WY) bulk_s2g(dst + SL_T, img + (OFF_T - OFF_IMG), 8192);  // T
     bulk_commit();
 }
 static_assert(SL_KG == 32768 && SL_U == 49152 && SL_D == 65536 && SL_AQK > SL_D, "slot layout used by the stores");
@@ -537,6 +548,7 @@ __device__ __forceinline__ void issue_loads(const Params &p, unsigned char *smem
 // finished chunk stays unpublished (and tasks drawn but not started wait on
 // nothing: the lowest-numbered unpublished task can always proceed).
 // Returns false when the slot wait gave up (timeout or abort).
+template <bool WY>  // the consumers form the WY product
 __device__ __forceinline__ bool run_task(const Params &p, const Ring &Rg, unsigned char *smem, const Task &cur,
                                          const int32_t *cu_s, int jmax, const Task &nxt, Task &nxt2, Cursor &cs, int &pending,
                                          int pending_val, bool &gate_bad, float &vmax) {
@@ -699,7 +711,7 @@ __device__ __forceinline__ bool run_task(const Params &p, const Ring &Rg, unsign
     // REL_TID: publish the previous slot, then wait for this task's slot and
     // send the part of the image that is final already. SYNC_TID: draw.
     const bool slot_inb = checked(cur.k >= 0 && cur.k < p.C && cur.j >= 0, p.status);
-    unsigned char *dst = Rg.slots + static_cast<size_t>(slot_inb ? cur.k * RING + cur.j % RING : 0) * SLOT_BYTES;
+    unsigned char *dst = Rg.slots + static_cast<size_t>(slot_inb ? cur.k * RING + cur.j % RING : 0) * SLOT_STRIDE<WY>;
     if (tid == REL_TID) {
         if (pending >= 0) {
             bulk_wait_all();
@@ -815,7 +827,10 @@ __device__ __forceinline__ bool run_task(const Params &p, const Ring &Rg, unsign
 #pragma unroll
             for (int r = 0; r < 16; ++r) {
                 vmax = max_abs_nan(vmax, x[r]);
-                sT[(16 * i + r) * RSA + 16 * i + jc] = __float2half_rn(x[r]);
+                if constexpr (WY)
+                    *reinterpret_cast<__half *>(smem + OFF_T + tile_elem(64, 16 * i + r, 16 * i + jc)) = __float2half_rn(x[r]);
+                else
+                    sT[(16 * i + r) * RSA + 16 * i + jc] = __float2half_rn(x[r]);
             }
         }
         if (lane == 0) KDA_TRACE_ANY(p, 50 + i, 0);
@@ -828,6 +843,56 @@ __device__ __forceinline__ bool run_task(const Params &p, const Ring &Rg, unsign
     if (!slot_ok) return false;
     KDA_TRACE_EV(p, 23, 0);
 
+    if constexpr (WY) {
+        // ---- step 3b alone (the consumers form the WY product): block
+        // diagonal d of T on warps 0 .. 3-d, block (w + d, w) on warp w,
+        // T_ij = -T_ii * sum_{k=j}^{i-1} L_ik T_kj, in the swizzled tile the
+        // late store sends
+        unsigned char *sTw = smem + OFF_T;
+        if (warp < 3) {
+#pragma unroll
+            for (int d = 1; d < 4; ++d) {
+                if (warp < 4 - d) {
+                    const int j = warp, i = warp + d;
+                    float m[2][4] = {};
+                    for (int kb = j; kb < i; ++kb) {
+                        uint32_t fa[4], fb[4];
+                        ldsm_x4(fa, sL + (16 * i + (lane & 15)) * RSA + 16 * kb + ((lane >> 4) << 3));
+                        ldsm_x4_t(fb, sTw + bk_addr(lane, 64, 16 * kb, 16 * j));
+                        mma16816_f16(m[0], fa, fb[0], fb[1]);
+                        mma16816_f16(m[1], fa, fb[2], fb[3]);
+                    }
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                        for (int hf = 0; hf < 2; ++hf) {
+                            vmax = max_abs_nan(max_abs_nan(vmax, m[nt][2 * hf]), m[nt][2 * hf + 1]);
+                            *reinterpret_cast<uint32_t *>(sTw + tile_elem(64, 16 * i + gq + 8 * hf, 16 * j + 8 * nt + 2 * qd)) =
+                                pack_f16(m[nt][2 * hf], m[nt][2 * hf + 1]);
+                        }
+                    __syncwarp();
+                    float t[2][4] = {};
+                    {
+                        uint32_t fa[4], fb[4];
+                        ldsm_x4(fa, sTw + a_addr(lane, 64, 16 * i, 16 * i));
+                        ldsm_x4_t(fb, sTw + bk_addr(lane, 64, 16 * i, 16 * j));
+                        mma16816_f16(t[0], fa, fb[0], fb[1]);
+                        mma16816_f16(t[1], fa, fb[2], fb[3]);
+                    }
+                    __syncwarp();
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                        for (int hf = 0; hf < 2; ++hf) {
+                            vmax = max_abs_nan(max_abs_nan(vmax, t[nt][2 * hf]), t[nt][2 * hf + 1]);
+                            *reinterpret_cast<uint32_t *>(sTw + tile_elem(64, 16 * i + gq + 8 * hf, 16 * j + 8 * nt + 2 * qd)) =
+                                pack_f16(-t[nt][2 * hf], -t[nt][2 * hf + 1]);
+                        }
+                }
+                if (d < 3) named_bar_sync(BAR_TB, 96);  // block diagonal d is complete
+            }
+        }
+    } else {
     // ---- steps 3b and 4, interleaved. Block row i of X = [u | w] =
     // T [beta v | beta k e^G] needs block rows 0..i of T = (I + L)^-1 only, so
     // while all warps compute X_i, warps 0 .. 2-i build block diagonal i+1 of T:
@@ -899,6 +964,7 @@ __device__ __forceinline__ bool run_task(const Params &p, const Ring &Rg, unsign
             if (xi < 3) sync_compute();  // block diagonal d of T is complete
         }
     }
+    }
     KDA_TRACE_EV(p, 24, 0);
     fence_proxy_async_shared();  // this thread's image writes, before the bulk store reads them
     sync_compute();
@@ -906,10 +972,11 @@ __device__ __forceinline__ bool run_task(const Params &p, const Ring &Rg, unsign
 
     // ---- hand-off: the rest of the image (published by REL_TID during the
     // next task's strips, or after the last task)
-    if (tid == REL_TID) store_late(dst, img);
+    if (tid == REL_TID) store_late<WY>(dst, img);
     return true;
 }
 
+template <bool WY>
 __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int pid) {
     const int tid = threadIdx.x;
     Ring R = ring_of(p);
@@ -929,6 +996,7 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int pi
         const int i = tile < 3 ? 0 : (tile < 5 ? 1 : 2);
         const int j = tile < 3 ? tile + 1 : (tile < 5 ? tile - 1 : 3);
         *reinterpret_cast<uint32_t *>(smem + OFF_IMG + SL_AQK + tile_elem(64, 16 * i + rr, 16 * j + cc)) = 0u;
+        if constexpr (WY) *reinterpret_cast<uint32_t *>(smem + OFF_T + tile_elem(64, 16 * i + rr, 16 * j + cc)) = 0u;  // and of T
     }
     sync_compute();
     const int jmax = misc[1];
@@ -953,7 +1021,7 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int pi
         sync_compute();
         KDA_TRACE_EV(p, 20, 0);
         Task nxt2{0, 0, 0, 0, 0, 0, 0, 0};
-        if (!run_task(p, R, smem, cur, cu_s, jmax, nxt, nxt2, cs, pending, pending_val, gate_bad, vmax))
+        if (!run_task<WY>(p, R, smem, cur, cu_s, jmax, nxt, nxt2, cs, pending, pending_val, gate_bad, vmax))
             break;
         if (tid == REL_TID) {
             pending = cur.k * RING + cur.j % RING;
@@ -985,14 +1053,21 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int pi
 //   MMA1  D  = [q_hat ; w] (K-major, 128 x 128) * S16 (fp16 snapshot, MN-major)
 //   MMA2  D += [scale*Aqk ; 0] (K-major, 128 x 64) * v_new (MN-major)   (lanes 0-63: o)
 //   MMA3  S += kg^T (MN-major, 128 x 64) * v_new, after S <- Diag(d) S in TMEM
+// When the consumers form the WY product (WY), A1 holds [q_hat ; beta k e^G]
+// and U holds beta v, so the v_new step yields Z = beta v - beta k e^G S, and
+//   MMAT  V  = [scale*Aqk ; T] (K-major, 128 x 64) * Z (MN-major)   (lanes 64-127: v_new = T Z)
+// goes into TMEM columns 256-383 before MMA2 and MMA3; the T tile then takes
+// the place of the zeros in MMA2, whose rows 64-127 land in the consumed
+// lanes 64-127 of D.
 namespace cons {
-constexpr int BUF_BYTES = SLOT_BYTES + 8192;   // slot + 8 KB of zeros: rows 64-127 of [Aqk; 0]
+constexpr int BUF_BYTES = SL_T + 8192;          // slot + 8 KB of zeros (or T): rows 64-127 of [Aqk; 0]
 constexpr int OFF_BUF0 = 0;
 constexpr int OFF_BUF1 = BUF_BYTES;             // 82944 (1024-aligned)
 constexpr int OFF_S = 2 * BUF_BYTES;            // S16: fp16 [key][value], MN-major swizzled, 32 KB
 constexpr int OFF_VN = OFF_S + 32768;           // v_new: fp16 [token][value], MN-major swizzled, 16 KB
 constexpr int OFF_BAR = OFF_VN + 16384;         // full[2], mma1, mma23
 constexpr int OFF_TMEM = OFF_BAR + 32;          // TMEM base address written by tcgen05.alloc
+constexpr int OFF_BAR_T = OFF_BAR + 40;         // WY: MMAT's barrier
 constexpr int OFF_MISC = OFF_BAR + 64;
 constexpr int SMEM = OFF_MISC + 64;
 constexpr uint32_t TMEM_COLS = 256;
@@ -1036,6 +1111,7 @@ __device__ __forceinline__ bool wait_all(const Ring &R, uint64_t *bar, uint32_t 
     return false;
 }
 
+template <bool WY>  // the consumers form the WY product
 __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int quad = warp & 3, slice = warp >> 2;  // TMEM lane quarter, 32-column value slice
@@ -1050,16 +1126,17 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
     unsigned char *sVN = smem + OFF_VN;
 
     for (int i = tid; i < 2 * 512; i += NCOMP)  // the two zero blocks
-        *reinterpret_cast<uint4 *>(smem + (i >> 9) * BUF_BYTES + SLOT_BYTES + (i & 511) * 16) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4 *>(smem + (i >> 9) * BUF_BYTES + SL_T + (i & 511) * 16) = make_uint4(0, 0, 0, 0);
     if (tid == 0) {
         mbar_init(&full[0], 1);
         mbar_init(&full[1], 1);
         mbar_init(bar_mma1, 1);
         mbar_init(bar_mma23, 1);
+        if constexpr (WY) mbar_init(reinterpret_cast<uint64_t *>(smem + OFF_BAR_T), 1);
         mbar_fence_init();
         misc[0] = 1;
     }
-    if (warp == 0) tmem_alloc(tslot, TMEM_COLS);
+    if (warp == 0) tmem_alloc(tslot, WY ? 2 * TMEM_COLS : TMEM_COLS);  // WY: + V
     fence_proxy_async_shared();
     tc_fence_before();
     sync_compute();
@@ -1075,15 +1152,15 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
     // `newest_elsewhere`: this thread's newest store group staged in the
     // other buffer and may go on.
     auto issue = [&](int jj, bool newest_elsewhere) {
-        const unsigned char *src = R.slots + static_cast<size_t>(k * RING + jj % RING) * SLOT_BYTES;
+        const unsigned char *src = R.slots + static_cast<size_t>(k * RING + jj % RING) * SLOT_STRIDE<WY>;
         unsigned char *dst = smem + ((jj & 1) ? OFF_BUF1 : OFF_BUF0);
         if (newest_elsewhere)
             asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
         else
             bulk_wait_read();
         fence_proxy_async_global();
-        mbar_arrive_expect_tx(&full[jj & 1], SLOT_BYTES);
-        bulk_g2s(dst, src, SLOT_BYTES, &full[jj & 1]);
+        mbar_arrive_expect_tx(&full[jj & 1], SLOT_STRIDE<WY>);
+        bulk_g2s(dst, src, SLOT_STRIDE<WY>, &full[jj & 1]);
     };
     bool issued_next = false;  // thread 0 only
     if (tid == 0 && total > 0) {
@@ -1223,6 +1300,7 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
             }
 
             // (4) v_new = u - w S (TMEM lanes 64-127) -> fp16 [token][value] tile
+            // (WY: Z = beta v - beta k e^G S, the same arithmetic)
             wait_all(R, bar_mma1, j & 1, p.status);
             tc_fence_after();
             KDA_TRACE_EV(p, 14, j);
@@ -1256,6 +1334,45 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
             fence_proxy_async_shared();
             tc_fence_before();
             sync_compute();
+            if constexpr (WY) {
+                // (4b) MMAT: V = [scale*Aqk ; T] Z; v_new = V (lanes 64-127) -> the v_new tile
+                uint64_t *bar_t = reinterpret_cast<uint64_t *>(smem + OFF_BAR_T);
+                if (tid == 0) {
+                    tc_fence_after();
+                    const uint32_t aq = smem_u32(bb + SL_AQK), vn = smem_u32(sVN);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        umma_f16(tmem + 256, umma_desc_sw128(aq + kk * 32, 16, 1024), umma_desc_sw128(vn + kk * 2048, 8192, 1024),
+                                 idesc_av, kk > 0);
+                    umma_commit(bar_t);
+                }
+                wait_all(R, bar_t, j & 1, p.status);
+                tc_fence_after();
+                if (quad >= 2) {
+                    const int t = row - 64;
+#pragma unroll
+                    for (int cb = 0; cb < 2; ++cb) {  // 16 columns at a time
+                        uint32_t r[16];
+                        tmem_ld16(tS + 256 + 16 * cb, r);
+                        tmem_wait_ld();
+                        const int c8 = 32 * slice + 16 * cb;
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh) {
+                            uint32_t vp[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float y0 = __uint_as_float(r[8 * hh + 2 * e]), y1 = __uint_as_float(r[8 * hh + 2 * e + 1]);
+                                vmax = max_abs_nan(max_abs_nan(vmax, y0), y1);
+                                vp[e] = pack_f16(y0, y1);
+                            }
+                            *reinterpret_cast<uint4 *>(sVN + tile_chunk(64, t, c8 + 8 * hh)) = make_uint4(vp[0], vp[1], vp[2], vp[3]);
+                        }
+                    }
+                }
+                fence_proxy_async_shared();
+                tc_fence_before();
+                sync_compute();
+            }
             KDA_TRACE_EV(p, 15, j);
 
             // (5) MMA2: D[0:64] += (scale Aqk) v_new ; MMA3: S += kg^T v_new
@@ -1411,7 +1528,7 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
     tc_fence_before();
     sync_compute();
     tc_fence_after();
-    if (warp == 0) tmem_dealloc(tmem, TMEM_COLS);
+    if (warp == 0) tmem_dealloc(tmem, WY ? 2 * TMEM_COLS : TMEM_COLS);
 }
 }  // namespace cons
 
@@ -1426,6 +1543,7 @@ constexpr int SMEM_MAX = SMEM_TILES;
 #endif
 static_assert(SMEM_MAX <= 232448, "shared memory budget");
 
+template <bool WY>  // the consumers form the WY product
 __global__ void __launch_bounds__(NTHREADS, 1) kda_persistent_kernel(const __grid_constant__ Params p) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -1435,9 +1553,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_persistent_kernel(const __gri
 #endif
     build_sched(p, smem + OFF_SCHED, smem);  // the roles' tiles serve as scratch until it returns
     if (static_cast<int>(blockIdx.x) < p.C)
-        cons::run(p, smem, blockIdx.x);
+        cons::run<WY>(p, smem, blockIdx.x);
     else
-        prod::run(p, smem, blockIdx.x - p.C);
+        prod::run<WY>(p, smem, blockIdx.x - p.C);
 }
 
 // ------------------------------------------------------------------ host side
@@ -1518,6 +1636,25 @@ int consumers_for(int64_t chains, int64_t tokens, int64_t seqs, int grid) {
     return best;
 }
 
+// Whether the consumers form the WY product X = T [beta v | beta k e^G]. Only
+// a batch whose sequences can all have one length (tokens divisible by seqs)
+// qualifies, judged with that length by the same kind of estimate: a producer
+// task takes about 6.8 us (6.5 when the consumers do the WY product) and a
+// consumer chunk about 2.5 us (3.05), and the launch about the longer of
+// (busiest consumer's chunks) x (chunk time) and (all chunks) x (task time) /
+// (producer CTAs); the consumers' time is counted 1.25 times so that they keep
+// slack. (A batch of unequal lengths that still passes runs correctly, only
+// perhaps slower.)
+bool wy_for(int64_t chains, int64_t tokens, int64_t seqs, int C, int grid) {
+    if (seqs < 1 || tokens < 1 || tokens % seqs != 0 || C < 1 || C >= grid) return false;
+    const double per_chain = static_cast<double>((tokens / seqs + BT - 1) / BT);
+    const double busiest = static_cast<double>((chains + C - 1) / C) * per_chain;
+    const double per_prod = static_cast<double>(chains) * per_chain / static_cast<double>(grid - C);
+    const double t_prod = std::fmax(2.5 * busiest, 6.8 * per_prod);
+    const double t_cons = std::fmax(1.25 * 3.05 * busiest, 6.5 * per_prod);
+    return t_cons < t_prod;
+}
+
 size_t workspace_bytes(int64_t chains) {
     const int sms = num_sms();
     if (sms < 2 || chains < 1) return 0;
@@ -1532,17 +1669,22 @@ size_t workspace_bytes(int64_t chains) {
 cudaError_t launch(Params p, size_t ws_bytes, cudaStream_t stream) {
     const int sms = num_sms();
     if (sms < 2) return cudaErrorInvalidDevice;
-    cudaError_t e = cudaFuncSetAttribute(kda_persistent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_MAX);
-    if (e != cudaSuccess) return e;
-    int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kda_persistent_kernel, NTHREADS, SMEM_MAX);
-    if (e != cudaSuccess) return e;
-    if (per_sm < 1) return cudaErrorInvalidConfiguration;
     const int grid = sms;  // one CTA per SM; all co-resident (cooperative launch)
     const int64_t chains = static_cast<int64_t>(p.N) * p.H;
     p.C = consumers_for(chains, p.T, p.N, grid);
     p.Cws = max_consumers(chains, grid);
-    p.spin = p.debug ? SPIN_LIMIT_DEBUG : SPIN_LIMIT;
+    p.spin = (p.debug & KDA_DEBUG_WITHHOLD_READY) ? SPIN_LIMIT_DEBUG : SPIN_LIMIT;
+    bool wy = wy_for(chains, p.T, p.N, p.C, grid);
+    if (p.debug & KDA_DEBUG_WY_PRODUCER) wy = false;
+    if (p.debug & KDA_DEBUG_WY_CONSUMER) wy = true;
+    const void *kernel = wy ? reinterpret_cast<const void *>(kda_persistent_kernel<true>)
+                            : reinterpret_cast<const void *>(kda_persistent_kernel<false>);
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_MAX);
+    if (e != cudaSuccess) return e;
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, NTHREADS, SMEM_MAX);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
     if (ws_bytes < ring_offset(p.Cws) + static_cast<size_t>(p.Cws) * RING * SLOT_BYTES) return cudaErrorInvalidValue;
     // a plain o in device memory leaves full chunks by tensor stores (else, and
     // for partial chunks, by the warps: an o in mapped host memory, for one)
@@ -1561,8 +1703,7 @@ cudaError_t launch(Params p, size_t ws_bytes, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
 #endif
     void *args[] = {&p};
-    return cudaLaunchCooperativeKernel(reinterpret_cast<void *>(kda_persistent_kernel), dim3(grid), dim3(NTHREADS),
-                                       args, SMEM_MAX, stream);
+    return cudaLaunchCooperativeKernel(kernel, dim3(grid), dim3(NTHREADS), args, SMEM_MAX, stream);
 }
 
 }  // namespace pers

@@ -10,7 +10,7 @@ namespace kda {
 namespace pers {
 
 constexpr int RING = 4;              // ring slots per consumer
-constexpr int SLOT_BYTES = 74752;    // one (chain, chunk) hand-off, 1024-byte multiple
+constexpr int SLOT_BYTES = 82944;    // one (chain, chunk) hand-off at most, 1024-byte multiple
 
 struct Params {
     const __nv_bfloat16 *q, *k, *v;

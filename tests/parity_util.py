@@ -102,9 +102,10 @@ def check_guard(flat, what: str):
         f"{what}: a kernel wrote into the guard band around the output"
 
 
-def run_gpu(inp: dict, device="cuda", check=True, output_final_state=True):
-    """kda_chunk_fwd through the C ABI into outputs surrounded by NaN guard
-    bands, which are checked to be untouched afterwards."""
+def run_gpu(inp: dict, device="cuda", check=True, output_final_state=True, debug_flags: int = 0):
+    """kda_chunk_fwd (kda_chunk_fwd_debug with nonzero ``debug_flags``) through
+    the C ABI into outputs surrounded by NaN guard bands, which are checked to
+    be untouched afterwards."""
     from kda_chunked_prefill_gb300 import _lib
     d = to_device(inp, device)
     T, H, D = inp["q"].shape
@@ -113,7 +114,7 @@ def run_gpu(inp: dict, device="cuda", check=True, output_final_state=True):
     fs_flat, fs = _guarded((N, H, D, D), device) if output_final_state else (None, None)
     status = torch.zeros(1, dtype=torch.int32, device=device) if check else None
     _lib.kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], d["initial_state"],
-                       inp["scale"], inp["lower_bound"], o, fs, status)
+                       inp["scale"], inp["lower_bound"], o, fs, status, debug_flags=debug_flags)
     torch.cuda.synchronize()
     if check:
         code = int(status.item())

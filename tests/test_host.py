@@ -99,8 +99,19 @@ def _call_debug(lib, flags, **over):
 
 
 def test_debug_entry_rejects_unknown_flags(lib):
-    assert _call_debug(lib, 2) == kda.KDA_ERR_INVALID_ARG
+    assert _call_debug(lib, 8) == kda.KDA_ERR_INVALID_ARG
     assert _call_debug(lib, 0x80000001) == kda.KDA_ERR_INVALID_ARG
+    # the two WY placements exclude each other
+    assert _call_debug(lib, kda.KDA_DEBUG_WY_PRODUCER | kda.KDA_DEBUG_WY_CONSUMER) == kda.KDA_ERR_INVALID_ARG
+
+
+def test_debug_entry_accepts_each_wy_placement(lib):
+    for flags in (kda.KDA_DEBUG_WY_PRODUCER, kda.KDA_DEBUG_WY_CONSUMER,
+                  kda.KDA_DEBUG_WY_CONSUMER | kda.KDA_DEBUG_WITHHOLD_READY):
+        # validation runs first: a bad head size is still refused as such, and an empty call succeeds
+        assert _call_debug(lib, flags, dk=64) == kda.KDA_ERR_UNSUPPORTED
+        assert _call_debug(lib, flags, N=0, T=0, q=None, k=None, v=None, g=None,
+                           beta=None, o=None, cu=None) == kda.KDA_OK
 
 
 def test_debug_entry_validates_like_the_plain_call(lib):
