@@ -360,7 +360,8 @@ kda_status_t kda_chunk_fwd_static_scratch(const void *q, const void *k, const vo
  *                             final_state within the parity bar; a launch
  *                             normally picks one from the batch's shape (the
  *                             consumers' form only where all sequences can be
- *                             of one length and the consumers have slack).
+ *                             of one length, o is a plain device array (no
+ *                             gated norm) and the consumers have slack).
  *                             Setting both returns KDA_ERR_INVALID_ARG.
  *
  * With KDA_DEBUG_WITHHOLD_READY set, a wait gives up after 2^14 polls

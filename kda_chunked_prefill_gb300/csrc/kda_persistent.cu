@@ -1674,17 +1674,6 @@ cudaError_t launch(Params p, size_t ws_bytes, cudaStream_t stream) {
     p.C = consumers_for(chains, p.T, p.N, grid);
     p.Cws = max_consumers(chains, grid);
     p.spin = (p.debug & KDA_DEBUG_WITHHOLD_READY) ? SPIN_LIMIT_DEBUG : SPIN_LIMIT;
-    bool wy = wy_for(chains, p.T, p.N, p.C, grid);
-    if (p.debug & KDA_DEBUG_WY_PRODUCER) wy = false;
-    if (p.debug & KDA_DEBUG_WY_CONSUMER) wy = true;
-    const void *kernel = wy ? reinterpret_cast<const void *>(kda_persistent_kernel<true>)
-                            : reinterpret_cast<const void *>(kda_persistent_kernel<false>);
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_MAX);
-    if (e != cudaSuccess) return e;
-    int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, NTHREADS, SMEM_MAX);
-    if (e != cudaSuccess) return e;
-    if (per_sm < 1) return cudaErrorInvalidConfiguration;
     if (ws_bytes < ring_offset(p.Cws) + static_cast<size_t>(p.Cws) * RING * SLOT_BYTES) return cudaErrorInvalidValue;
     // a plain o in device memory leaves full chunks by tensor stores (else, and
     // for partial chunks, by the warps: an o in mapped host memory, for one)
@@ -1695,6 +1684,19 @@ cudaError_t launch(Params p, size_t ws_bytes, cudaStream_t stream) {
         (void)cudaGetLastError();  // clear a failed query
     }
     p.o_tma = (o_device && !p.ngate && encode_o(&p.tm_o, p.o, p.Ttok, p.H)) ? 1 : 0;
+    // the consumers take the WY product only with o on tensor stores (the
+    // warps' own o stores, and the gated norm, leave them no slack for it)
+    bool wy = p.o_tma && wy_for(chains, p.T, p.N, p.C, grid);
+    if (p.debug & KDA_DEBUG_WY_PRODUCER) wy = false;
+    if (p.debug & KDA_DEBUG_WY_CONSUMER) wy = true;
+    const void *kernel = wy ? reinterpret_cast<const void *>(kda_persistent_kernel<true>)
+                            : reinterpret_cast<const void *>(kda_persistent_kernel<false>);
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_MAX);
+    if (e != cudaSuccess) return e;
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, NTHREADS, SMEM_MAX);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
     e = cudaMemsetAsync(p.ws, 0, ring_offset(p.C), stream);
     if (e != cudaSuccess) return e;
 #ifdef KDA_TRACE
