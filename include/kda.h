@@ -87,8 +87,8 @@ typedef enum {
  *   initial_state fp32 [num_seqs, num_heads, 128, 128] (S[i][j], i = key
  *                 channel, j = value channel), or NULL for zeros.
  *   scale         multiplies o only (typically 128^-0.5).
- *   lower_bound   the gate's lower bound; must lie in [-10.9, 0] so that the
- *                 sub-block factors stay below 2^126.
+ *   lower_bound   the gate's lower bound; must lie in [-10, 0) so that the
+ *                 sub-block factors 2^(8 |lower_bound| / ln 2) stay below 2^126.
  * Outputs:
  *   o             fp32 [total_tokens, num_heads, 128]. (fp32 rather than bf16: a
  *                 bf16 o alone would round the largest outputs by up to 2^-9 of

@@ -13,9 +13,10 @@ constexpr int64_t kMaxTokens = 0x7fffffffLL - 64;
 
 inline bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// The strip products form factors up to 2^(8 |lower_bound| / ln 2); keep that
-// below 2^126 so they stay finite in bf16 and fp32.
-inline bool lower_bound_ok(float lb) { return lb >= -10.9f && lb <= 0.0f; }
+// The strip products form factors up to 2^(8 |lower_bound| / ln 2); the bound
+// lies in [-10, 0) so that they stay below 2^126 (finite in bf16 and fp32)
+// with a margin.
+inline bool lower_bound_ok(float lb) { return lb >= -10.0f && lb < 0.0f; }
 
 inline bool scale_ok(float s) { return s == s; }
 

@@ -103,7 +103,7 @@ extern "C" kda_status_t kda_decode_fwd(const void *q, const void *k, const void 
     if (num_seqs < 0 || num_heads < 1 || tokens_per_seq < 0 || tokens_per_seq > KDA_DECODE_MAX_TOKENS)
         return KDA_ERR_INVALID_ARG;
     if (static_cast<int64_t>(num_seqs) * num_heads * 4 > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
-    if (!(scale == scale) || !(lower_bound >= -10.9f && lower_bound <= 0.0f)) return KDA_ERR_INVALID_ARG;
+    if (!(scale == scale) || !(lower_bound >= -10.0f && lower_bound < 0.0f)) return KDA_ERR_INVALID_ARG;
     if (num_seqs == 0) return KDA_OK;
     if (tokens_per_seq > 0) {
         if (!q || !k || !v || !g || !beta || !o) return KDA_ERR_INVALID_ARG;

@@ -70,6 +70,8 @@ def _call(lib, **over):
     ({"T": -5}, kda.KDA_ERR_INVALID_ARG),
     ({"lb": -20.0}, kda.KDA_ERR_INVALID_ARG),
     ({"lb": 0.5}, kda.KDA_ERR_INVALID_ARG),
+    ({"lb": 0.0}, kda.KDA_ERR_INVALID_ARG),     # the bound lies in [-10, 0)
+    ({"lb": -10.5}, kda.KDA_ERR_INVALID_ARG),
     ({"scale": float("nan")}, kda.KDA_ERR_INVALID_ARG),
     ({"q": None}, kda.KDA_ERR_INVALID_ARG),
     ({"g": None}, kda.KDA_ERR_INVALID_ARG),
@@ -276,6 +278,7 @@ def _call_decode(lib, **over):
     ({"Tn": -1}, kda.KDA_ERR_INVALID_ARG),
     ({"Tn": 65}, kda.KDA_ERR_INVALID_ARG),  # beyond KDA_DECODE_MAX_TOKENS
     ({"lb": -11.0}, kda.KDA_ERR_INVALID_ARG),
+    ({"lb": 0.0}, kda.KDA_ERR_INVALID_ARG),
     ({"scale": float("nan")}, kda.KDA_ERR_INVALID_ARG),
     ({"q": None}, kda.KDA_ERR_INVALID_ARG),
     ({"o": None}, kda.KDA_ERR_INVALID_ARG),
