@@ -233,6 +233,25 @@ kda_status_t kda_chunk_fwd_split(const void *q, const void *k, const void *v, co
                                  float *o, float *final_state, int32_t *status_dev, void *workspace,
                                  size_t workspace_bytes, kda_stream_t stream);
 
+/* How kda_chunk_fwd lays out a call of num_seqs sequences, total_tokens tokens
+ * and num_heads heads on a GPU with num_sms SMs (0: the current device), with
+ * one CTA per SM:
+ *   *consumers        the CTAs that carry the chains' recurrence (the others
+ *                     run the intra-chunk steps for them);
+ *   *wy_on_consumers  1 when those consumers also form the WY product
+ *                     X = T [beta v | beta k e^G] (the producers then send T),
+ *                     0 when the producers form it.
+ * plain_device_o: 1 for an o in device memory without the gated norm (full
+ * chunks of o leave by tensor stores), 0 otherwise; the consumers take the WY
+ * product only in the first case. Host only; nothing is launched. Returns
+ * KDA_OK; KDA_ERR_INVALID_ARG for num_seqs or num_heads below 1, a negative
+ * total_tokens or num_sms, or a NULL output; KDA_ERR_UNSUPPORTED for fewer than
+ * two SMs; KDA_ERR_CUDA when num_sms is 0 and no device answers.
+ * (Not part of the method: the pages define no counterpart.)
+ */
+kda_status_t kda_chunk_fwd_plan(int32_t num_seqs, int64_t total_tokens, int32_t num_heads, int32_t num_sms,
+                                int32_t plain_device_o, int32_t *consumers, int32_t *wy_on_consumers);
+
 /* The segment length (chunks) kda_chunk_fwd_split picks for these lengths on a
  * GPU with num_sms SMs (0: the current device), from the measured paces of the
  * chunked kernel (a busy consumer SM finishes a chunk every 3.5 us, a producer

@@ -10,7 +10,7 @@ from __future__ import annotations
 import ctypes
 import os
 import threading
-from typing import Optional
+from typing import Optional, Tuple
 
 import torch
 
@@ -33,7 +33,7 @@ KDA_DEBUG_WY_CONSUMER = 4  # the consumer CTAs form it
 HEAD_DIM = 128
 EXPORTED = ("kda_chunk_fwd", "kda_chunk_fwd_workspace_size", "kda_chunk_fwd_static_scratch",
             "kda_chunk_fwd_debug", "kda_chunk_fwd_raw_gates", "kda_chunk_fwd_gated_norm", "kda_chunk_fwd_split",
-            "kda_chunk_fwd_split_plan", "kda_chunk_fwd_split_workspace_size", "kda_chunk_fwd_host",
+            "kda_chunk_fwd_split_plan", "kda_chunk_fwd_split_workspace_size", "kda_chunk_fwd_host", "kda_chunk_fwd_plan",
             "kda_chunk_fwd_host_buffer_size", "kda_decode_fwd",
             "kda_chunk_fwd_launches",
             "kda_status_string", "kda_version")
@@ -82,6 +82,8 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.kda_chunk_fwd_split.restype = ctypes.c_int
         lib.kda_chunk_fwd_split_plan.argtypes = [vp, i32, i32, i32]
         lib.kda_chunk_fwd_split_plan.restype = ctypes.c_int32
+        lib.kda_chunk_fwd_plan.argtypes = [i32, i64, i32, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32)]
+        lib.kda_chunk_fwd_plan.restype = ctypes.c_int
         lib.kda_chunk_fwd_split_workspace_size.argtypes = [vp, i32, i32, i32]
         lib.kda_chunk_fwd_split_workspace_size.restype = ctypes.c_size_t
         lib.kda_chunk_fwd_host.argtypes = [vp, vp, vp, vp, vp, vp, i32, i64, i32, i32, i32, vp, f32, f32, vp, vp, vp,
@@ -268,6 +270,18 @@ def split_plan(cu_seqlens_host, num_heads: int, num_sms: int = 0) -> int:
     for these sequence lengths (0: no split). ``num_sms`` 0 = the current device."""
     cu, ptr = _host_cu(cu_seqlens_host)
     return int(load_library().kda_chunk_fwd_split_plan(ptr, cu.numel() - 1, int(num_heads), int(num_sms)))
+
+
+def chunk_fwd_plan(num_seqs: int, total_tokens: int, num_heads: int, num_sms: int = 0,
+                   plain_device_o: bool = True) -> Tuple[int, bool]:
+    """``kda_chunk_fwd_plan``: (consumer CTAs, whether the consumers form the WY
+    product) for a call of this shape. ``num_sms`` 0 = the current device."""
+    c, w = ctypes.c_int32(0), ctypes.c_int32(0)
+    rc = load_library().kda_chunk_fwd_plan(int(num_seqs), int(total_tokens), int(num_heads), int(num_sms),
+                                           1 if plain_device_o else 0, ctypes.byref(c), ctypes.byref(w))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_chunk_fwd_plan")
+    return int(c.value), bool(w.value)
 
 
 def split_workspace_size(cu_seqlens_host, num_heads: int, segment_chunks: int = 0) -> int:

@@ -127,6 +127,27 @@ kda_status_t kda_chunk_fwd(const void *q, const void *k, const void *v, const fl
                     stream);
 }
 
+kda_status_t kda_chunk_fwd_plan(int32_t num_seqs, int64_t total_tokens, int32_t num_heads, int32_t num_sms,
+                                int32_t plain_device_o, int32_t *consumers, int32_t *wy_on_consumers) {
+    if (num_seqs < 1 || num_heads < 1 || total_tokens < 0 || num_sms < 0 || !consumers || !wy_on_consumers)
+        return KDA_ERR_INVALID_ARG;
+    int sms = num_sms;
+    if (sms == 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return KDA_ERR_CUDA;
+        }
+    }
+    if (sms < 2) return KDA_ERR_UNSUPPORTED;
+    // the same two choices the launch makes (one CTA per SM)
+    const int64_t chains = static_cast<int64_t>(num_seqs) * num_heads;
+    const int C = kda::pers::consumers_for(chains, total_tokens, num_seqs, sms);
+    *consumers = C;
+    *wy_on_consumers = (plain_device_o && kda::pers::wy_for(chains, total_tokens, num_seqs, C, sms)) ? 1 : 0;
+    return KDA_OK;
+}
+
 kda_status_t kda_chunk_fwd_debug(const void *q, const void *k, const void *v, const float *g,
                                  const float *beta, const int32_t *cu_seqlens, int32_t num_seqs,
                                  int64_t total_tokens, int32_t num_heads, int32_t head_dim_k,

@@ -51,6 +51,7 @@ __host__ __device__ constexpr size_t ring_offset(int C) {
 
 int max_consumers(int64_t chains, int grid);
 int consumers_for(int64_t chains, int64_t tokens, int64_t seqs, int grid);
+bool wy_for(int64_t chains, int64_t tokens, int64_t seqs, int C, int grid);
 size_t workspace_bytes(int64_t chains);
 cudaError_t launch(Params p, size_t ws_bytes, cudaStream_t stream);
 

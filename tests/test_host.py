@@ -302,3 +302,32 @@ def test_empty_problem_is_a_no_op(lib):
     assert _call(lib, N=0, T=0, q=None, k=None, v=None, g=None, beta=None, o=None, cu=None) == kda.KDA_OK
     assert kda.chunk_fwd_launches(0, 0, 4) == 0
     assert kda.chunk_fwd_launches(4, 8192, 16) == 1
+
+
+# ---- kda_chunk_fwd_plan: the launch's two choices, on the host
+@pytest.mark.parametrize("shape,sms,plain,expect", [
+    ((4, 8192, 16), 152, True, (64, True)),     # the equal-length batch: consumers have slack
+    ((4, 8192, 16), 152, False, (64, False)),   # o not on tensor stores: the producers keep it
+    ((1, 16384, 96), 152, True, (48, False)),   # two chains per consumer: consumer-bound
+    ((3, 24576, 96), 152, True, (48, False)),
+    ((1, 65536, 4), 152, True, (4, False)),     # few long chains
+    ((4, 4390, 16), 152, True, (64, False)),    # lengths cannot all be equal
+    ((16, 12091, 16), 152, True, (52, False)),
+    ((1, 256, 2), 152, True, (2, False)),
+])
+def test_plan_matches_the_launch_rule(lib, shape, sms, plain, expect):
+    assert kda.chunk_fwd_plan(*shape, num_sms=sms, plain_device_o=plain) == expect
+
+
+def test_plan_rejects_bad_arguments(lib):
+    c, w = ctypes.c_int32(0), ctypes.c_int32(0)
+    ok = (ctypes.byref(c), ctypes.byref(w))
+    assert lib.kda_chunk_fwd_plan(0, 100, 4, 152, 1, *ok) == kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_chunk_fwd_plan(2, 100, 0, 152, 1, *ok) == kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_chunk_fwd_plan(2, -1, 4, 152, 1, *ok) == kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_chunk_fwd_plan(2, 100, 4, -1, 1, *ok) == kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_chunk_fwd_plan(2, 100, 4, 152, 1, None, ctypes.byref(w)) == kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_chunk_fwd_plan(2, 100, 4, 1, 1, *ok) == kda.KDA_ERR_UNSUPPORTED
+    import torch
+    if not torch.cuda.is_available():  # the current device is asked for its SM count
+        assert lib.kda_chunk_fwd_plan(2, 100, 4, 0, 1, *ok) == kda.KDA_ERR_CUDA
