@@ -38,3 +38,11 @@ def test_wy_placement_matches_the_oracle(flags, case):
     pu.assert_parity(o.cpu().numpy(), ref_o, f"o (flags {flags})")
     pu.assert_parity(fs.cpu().numpy(), ref_s, f"final_state (flags {flags})")
 
+
+
+def test_plan_on_this_device():
+    # num_sms = 0 asks the current device; on it, the plan is the one for its SM count
+    import torch
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for shape in ((4, 8192, 16), (1, 16384, 96), (16, 12091, 16)):
+        assert kda.chunk_fwd_plan(*shape) == kda.chunk_fwd_plan(*shape, num_sms=sms)
