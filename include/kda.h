@@ -236,21 +236,26 @@ kda_status_t kda_chunk_fwd_split(const void *q, const void *k, const void *v, co
 /* How kda_chunk_fwd lays out a call of num_seqs sequences, total_tokens tokens
  * and num_heads heads on a GPU with num_sms SMs (0: the current device), with
  * one CTA per SM:
- *   *consumers        the CTAs that carry the chains' recurrence (the others
- *                     run the intra-chunk steps for them);
+ *   *consumers        the consumers that carry the chains' recurrence (the
+ *                     other CTAs run the intra-chunk steps for them);
  *   *wy_on_consumers  1 when those consumers also form the WY product
  *                     X = T [beta v | beta k e^G] (the producers then send T),
- *                     0 when the producers form it.
+ *                     0 when the producers form it;
+ *   *split_columns    1 when each consumer is a pair of CTAs taking one half of
+ *                     the 128 value columns each (then one chain per consumer),
+ *                     0 when it is one CTA.
  * plain_device_o: 1 for an o in device memory without the gated norm (full
  * chunks of o leave by tensor stores), 0 otherwise; the consumers take the WY
- * product only in the first case. Host only; nothing is launched. Returns
+ * product only in the first case. (The gated norm never splits columns; this
+ * call does not model it.) Host only; nothing is launched. Returns
  * KDA_OK; KDA_ERR_INVALID_ARG for num_seqs or num_heads below 1, a negative
  * total_tokens or num_sms, or a NULL output; KDA_ERR_UNSUPPORTED for fewer than
  * two SMs; KDA_ERR_CUDA when num_sms is 0 and no device answers.
  * (Not part of the method: the pages define no counterpart.)
  */
 kda_status_t kda_chunk_fwd_plan(int32_t num_seqs, int64_t total_tokens, int32_t num_heads, int32_t num_sms,
-                                int32_t plain_device_o, int32_t *consumers, int32_t *wy_on_consumers);
+                                int32_t plain_device_o, int32_t *consumers, int32_t *wy_on_consumers,
+                                int32_t *split_columns);
 
 /* The segment length (chunks) kda_chunk_fwd_split picks for these lengths on a
  * GPU with num_sms SMs (0: the current device), from the measured paces of the
@@ -382,6 +387,13 @@ kda_status_t kda_chunk_fwd_static_scratch(const void *q, const void *k, const vo
  *                             of one length, o is a plain device array (no
  *                             gated norm) and the consumers have slack).
  *                             Setting both returns KDA_ERR_INVALID_ARG.
+ *   KDA_DEBUG_SPLIT_COLUMNS   each chain's 128 value columns go to a pair of
+ *                             consumer CTAs, one half each, where every chain
+ *                             can have a pair within half the SMs (else the
+ *                             flag is ignored), whatever the launch's choice.
+ *   KDA_DEBUG_WHOLE_COLUMNS   one consumer CTA takes all of a chain's columns.
+ *                             Setting both, or KDA_DEBUG_SPLIT_COLUMNS with
+ *                             KDA_DEBUG_WY_CONSUMER, returns KDA_ERR_INVALID_ARG.
  *
  * With KDA_DEBUG_WITHHOLD_READY set, a wait gives up after 2^14 polls
  * (milliseconds) instead of 2^24; o and final_state are then unspecified.
@@ -392,6 +404,8 @@ kda_status_t kda_chunk_fwd_static_scratch(const void *q, const void *k, const vo
 #define KDA_DEBUG_WITHHOLD_READY 1u
 #define KDA_DEBUG_WY_PRODUCER 2u
 #define KDA_DEBUG_WY_CONSUMER 4u
+#define KDA_DEBUG_SPLIT_COLUMNS 8u
+#define KDA_DEBUG_WHOLE_COLUMNS 16u
 kda_status_t kda_chunk_fwd_debug(const void *q, const void *k, const void *v, const float *g,
                                  const float *beta, const int32_t *cu_seqlens, int32_t num_seqs,
                                  int64_t total_tokens, int32_t num_heads, int32_t head_dim_k,

@@ -29,6 +29,8 @@ KDA_ERR_BOUNDS = 9
 KDA_DEBUG_WITHHOLD_READY = 1
 KDA_DEBUG_WY_PRODUCER = 2  # the producer CTAs form the WY product
 KDA_DEBUG_WY_CONSUMER = 4  # the consumer CTAs form it
+KDA_DEBUG_SPLIT_COLUMNS = 8  # a chain's value columns over two consumer CTAs
+KDA_DEBUG_WHOLE_COLUMNS = 16  # one consumer CTA per chain's columns
 
 HEAD_DIM = 128
 EXPORTED = ("kda_chunk_fwd", "kda_chunk_fwd_workspace_size", "kda_chunk_fwd_static_scratch",
@@ -82,7 +84,8 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.kda_chunk_fwd_split.restype = ctypes.c_int
         lib.kda_chunk_fwd_split_plan.argtypes = [vp, i32, i32, i32]
         lib.kda_chunk_fwd_split_plan.restype = ctypes.c_int32
-        lib.kda_chunk_fwd_plan.argtypes = [i32, i64, i32, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32)]
+        lib.kda_chunk_fwd_plan.argtypes = [i32, i64, i32, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32),
+                                           ctypes.POINTER(i32)]
         lib.kda_chunk_fwd_plan.restype = ctypes.c_int
         lib.kda_chunk_fwd_split_workspace_size.argtypes = [vp, i32, i32, i32]
         lib.kda_chunk_fwd_split_workspace_size.restype = ctypes.c_size_t
@@ -273,15 +276,17 @@ def split_plan(cu_seqlens_host, num_heads: int, num_sms: int = 0) -> int:
 
 
 def chunk_fwd_plan(num_seqs: int, total_tokens: int, num_heads: int, num_sms: int = 0,
-                   plain_device_o: bool = True) -> Tuple[int, bool]:
-    """``kda_chunk_fwd_plan``: (consumer CTAs, whether the consumers form the WY
-    product) for a call of this shape. ``num_sms`` 0 = the current device."""
-    c, w = ctypes.c_int32(0), ctypes.c_int32(0)
+                   plain_device_o: bool = True) -> Tuple[int, bool, bool]:
+    """``kda_chunk_fwd_plan``: (consumers, whether the consumers form the WY
+    product, whether each consumer is two CTAs with half the value columns each)
+    for a call of this shape. ``num_sms`` 0 = the current device."""
+    c, w, sp = ctypes.c_int32(0), ctypes.c_int32(0), ctypes.c_int32(0)
     rc = load_library().kda_chunk_fwd_plan(int(num_seqs), int(total_tokens), int(num_heads), int(num_sms),
-                                           1 if plain_device_o else 0, ctypes.byref(c), ctypes.byref(w))
+                                           1 if plain_device_o else 0, ctypes.byref(c), ctypes.byref(w),
+                                           ctypes.byref(sp))
     if rc != KDA_OK:
         raise KdaError(rc, "kda_chunk_fwd_plan")
-    return int(c.value), bool(w.value)
+    return int(c.value), bool(w.value), bool(sp.value)
 
 
 def split_workspace_size(cu_seqlens_host, num_heads: int, segment_chunks: int = 0) -> int:

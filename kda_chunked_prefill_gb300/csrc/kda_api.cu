@@ -128,8 +128,10 @@ kda_status_t kda_chunk_fwd(const void *q, const void *k, const void *v, const fl
 }
 
 kda_status_t kda_chunk_fwd_plan(int32_t num_seqs, int64_t total_tokens, int32_t num_heads, int32_t num_sms,
-                                int32_t plain_device_o, int32_t *consumers, int32_t *wy_on_consumers) {
-    if (num_seqs < 1 || num_heads < 1 || total_tokens < 0 || num_sms < 0 || !consumers || !wy_on_consumers)
+                                int32_t plain_device_o, int32_t *consumers, int32_t *wy_on_consumers,
+                                int32_t *split_columns) {
+    if (num_seqs < 1 || num_heads < 1 || total_tokens < 0 || num_sms < 0 || !consumers || !wy_on_consumers ||
+        !split_columns)
         return KDA_ERR_INVALID_ARG;
     int sms = num_sms;
     if (sms == 0) {
@@ -143,8 +145,10 @@ kda_status_t kda_chunk_fwd_plan(int32_t num_seqs, int64_t total_tokens, int32_t 
     // the same two choices the launch makes (one CTA per SM)
     const int64_t chains = static_cast<int64_t>(num_seqs) * num_heads;
     const int C = kda::pers::consumers_for(chains, total_tokens, num_seqs, sms);
-    *consumers = C;
-    *wy_on_consumers = (plain_device_o && kda::pers::wy_for(chains, total_tokens, num_seqs, C, sms)) ? 1 : 0;
+    const bool split = kda::pers::split_for(chains, total_tokens, num_seqs, C, sms);
+    *consumers = split ? static_cast<int32_t>(chains) : C;
+    *split_columns = split ? 1 : 0;
+    *wy_on_consumers = (!split && plain_device_o && kda::pers::wy_for(chains, total_tokens, num_seqs, C, sms)) ? 1 : 0;
     return KDA_OK;
 }
 
@@ -155,8 +159,11 @@ kda_status_t kda_chunk_fwd_debug(const void *q, const void *k, const void *v, co
                                  float lower_bound, float *o, float *final_state,
                                  int32_t *status_dev, void *workspace, size_t workspace_bytes,
                                  kda_stream_t stream, uint32_t debug_flags) {
-    constexpr uint32_t known = KDA_DEBUG_WITHHOLD_READY | KDA_DEBUG_WY_PRODUCER | KDA_DEBUG_WY_CONSUMER;
-    if ((debug_flags & ~known) || ((debug_flags & KDA_DEBUG_WY_PRODUCER) && (debug_flags & KDA_DEBUG_WY_CONSUMER)))
+    constexpr uint32_t known = KDA_DEBUG_WITHHOLD_READY | KDA_DEBUG_WY_PRODUCER | KDA_DEBUG_WY_CONSUMER |
+                               KDA_DEBUG_SPLIT_COLUMNS | KDA_DEBUG_WHOLE_COLUMNS;
+    auto both = [&](uint32_t a, uint32_t b) { return (debug_flags & a) && (debug_flags & b); };
+    if ((debug_flags & ~known) || both(KDA_DEBUG_WY_PRODUCER, KDA_DEBUG_WY_CONSUMER) ||
+        both(KDA_DEBUG_SPLIT_COLUMNS, KDA_DEBUG_WHOLE_COLUMNS) || both(KDA_DEBUG_SPLIT_COLUMNS, KDA_DEBUG_WY_CONSUMER))
         return KDA_ERR_INVALID_ARG;
     Extras x;
     x.debug = debug_flags;

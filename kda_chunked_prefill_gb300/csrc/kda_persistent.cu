@@ -124,6 +124,7 @@ struct Ring {
     Header *hdr;
     int *ready;  // [C][RING]: chunk index + 1 held by the slot
     int *freed;  // [C][RING]: chunk index + 1 the consumer has copied out
+    int *freed2; // [C][RING]: the same for the second CTA of a consumer whose columns are split
     unsigned char *slots;
     long long spin;  // polls before a wait gives up
 };
@@ -133,6 +134,7 @@ __device__ __forceinline__ Ring ring_of(const Params &p) {
     r.hdr = reinterpret_cast<Header *>(p.ws);
     r.ready = reinterpret_cast<int *>(p.ws + sizeof(Header));
     r.freed = r.ready + p.C * RING;
+    r.freed2 = r.freed + p.C * RING;
     r.slots = p.ws + ring_offset(p.C);
     r.spin = p.spin;
     return r;
@@ -548,7 +550,7 @@ __device__ __forceinline__ void issue_loads(const Params &p, unsigned char *smem
 // finished chunk stays unpublished (and tasks drawn but not started wait on
 // nothing: the lowest-numbered unpublished task can always proceed).
 // Returns false when the slot wait gave up (timeout or abort).
-template <bool WY>  // the consumers form the WY product
+template <bool WY, bool HALF>  // the consumers form the WY product; each consumer is two CTAs (column halves)
 __device__ __forceinline__ bool run_task(const Params &p, const Ring &Rg, unsigned char *smem, const Task &cur,
                                          const int32_t *cu_s, int jmax, const Task &nxt, Task &nxt2, Cursor &cs, int &pending,
                                          int pending_val, bool &gate_bad, float &vmax) {
@@ -722,7 +724,8 @@ __device__ __forceinline__ bool run_task(const Params &p, const Ring &Rg, unsign
         KDA_TRACE_ANY(p, 31, 0);
         const int s = cur.j % RING;
         const bool free_ok =
-            slot_inb && ((cur.j < RING) || wait_flag_geq(Rg, &Rg.freed[cur.k * RING + s], cur.j - RING + 1, p.status));
+            slot_inb && ((cur.j < RING) || (wait_flag_geq(Rg, &Rg.freed[cur.k * RING + s], cur.j - RING + 1, p.status) &&
+                                            (!HALF || wait_flag_geq(Rg, &Rg.freed2[cur.k * RING + s], cur.j - RING + 1, p.status))));
         misc[20] = free_ok ? 1 : 0;
         if (free_ok) store_early(dst, img);
         KDA_TRACE_ANY(p, 33, 0);
@@ -976,7 +979,7 @@ __device__ __forceinline__ bool run_task(const Params &p, const Ring &Rg, unsign
     return true;
 }
 
-template <bool WY>
+template <bool WY, bool HALF>
 __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int pid) {
     const int tid = threadIdx.x;
     Ring R = ring_of(p);
@@ -1000,7 +1003,7 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int pi
     }
     sync_compute();
     const int jmax = misc[1];
-    Cursor cs = make_cursor(pid, static_cast<int>(gridDim.x) - p.C, p.C);  // used by SYNC_TID
+    Cursor cs = make_cursor(pid, static_cast<int>(gridDim.x) - (HALF ? 2 : 1) * p.C, p.C);  // used by SYNC_TID
     if (tid == SYNC_TID) {
         const Task t = fetch_task(p, smem, cu_s, jmax, cs);
         put_task(misc + 2, t);
@@ -1021,7 +1024,7 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int pi
         sync_compute();
         KDA_TRACE_EV(p, 20, 0);
         Task nxt2{0, 0, 0, 0, 0, 0, 0, 0};
-        if (!run_task<WY>(p, R, smem, cur, cu_s, jmax, nxt, nxt2, cs, pending, pending_val, gate_bad, vmax))
+        if (!run_task<WY, HALF>(p, R, smem, cur, cu_s, jmax, nxt, nxt2, cs, pending, pending_val, gate_bad, vmax))
             break;
         if (tid == REL_TID) {
             pending = cur.k * RING + cur.j % RING;
@@ -1111,10 +1114,15 @@ __device__ __forceinline__ bool wait_all(const Ring &R, uint64_t *bar, uint32_t 
     return false;
 }
 
-template <bool WY>  // the consumers form the WY product
-__device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k) {
+template <bool WY, bool HALF>  // the consumers form the WY product; this CTA is one column half
+__device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k, int half) {
+    // value columns of this CTA: all 128, or with HALF the half [v0, v0 + 64)
+    // (column j of v_new, o and S depends on column j of S alone)
+    constexpr int NV = HALF ? 64 : 128, NCT = NV / 4;  // columns of the CTA; of a thread's slice
+    const int v0 = HALF ? 64 * half : 0;
+    const __nv_bfloat16 *ngate = HALF ? nullptr : p.ngate;  // (a split consumer has no whole rows to norm)
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int quad = warp & 3, slice = warp >> 2;  // TMEM lane quarter, 32-column value slice
+    const int quad = warp & 3, slice = warp >> 2;  // TMEM lane quarter, NCT-column value slice
     const int row = 32 * quad + lane;             // this thread's TMEM lane
     Ring R = ring_of(p);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
@@ -1142,7 +1150,7 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
     sync_compute();
     tc_fence_after();
     const uint32_t tmem = *tslot;
-    const uint32_t tS = tmem + (static_cast<uint32_t>(32 * quad) << 16) + 32 * slice;  // this thread's S columns
+    const uint32_t tS = tmem + (static_cast<uint32_t>(32 * quad) << 16) + NCT * slice;  // this thread's S columns
     const uint32_t tD = tS + 128;                                                       // this thread's D columns
     const int32_t *cu_s = sched_cu(p, smem);
     const int total = consumer_total(p, smem, cu_s, k);
@@ -1169,9 +1177,9 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
         else
             misc[0] = 0;
     }
-    const uint32_t idesc_qw = umma_idesc_f16(false, true, 128, 128);  // [q_hat; w] x S16
-    const uint32_t idesc_av = umma_idesc_f16(false, true, 128, 128);  // [Aqk; 0] x v_new
-    const uint32_t idesc_kv = umma_idesc_f16(true, true, 128, 128);   // kg^T x v_new
+    const uint32_t idesc_qw = umma_idesc_f16(false, true, 128, NV);  // [q_hat; w] x S16
+    const uint32_t idesc_av = umma_idesc_f16(false, true, 128, NV);  // [Aqk; 0] x v_new
+    const uint32_t idesc_kv = umma_idesc_f16(true, true, 128, NV);   // kg^T x v_new
 
     int j = 0;
     bool alive = true;
@@ -1188,12 +1196,12 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
         const int n = ch / p.H, h = ch % p.H;
         const bool st_inb = checked(ch >= 0 && n < p.N, p.status);  // a failed check skips the state accesses
         const size_t state_base = st_inb ? (static_cast<size_t>(n) * p.H + h) * (DK * DV) : 0;
-        // initial state (or zeros) -> TMEM: row `row`, columns 32*slice..+31
+        // initial state (or zeros) -> TMEM: row `row`, columns v0 + NCT*slice .. +NCT-1
 #pragma unroll
-        for (int cb = 0; cb < 2; ++cb) {
+        for (int cb = 0; cb < NCT / 16; ++cb) {
             uint32_t r[16];
             if (p.s0 && st_inb) {
-                const float4 *src = reinterpret_cast<const float4 *>(p.s0 + state_base + row * DV + 32 * slice + 16 * cb);
+                const float4 *src = reinterpret_cast<const float4 *>(p.s0 + state_base + row * DV + v0 + NCT * slice + 16 * cb);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const float4 f = src[e];
@@ -1221,7 +1229,7 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
                 if (was_alive && wait_mbar(R, &full[b], (j >> 1) & 1, p.status)) {
                     // the copy of slot j has completed (its reads are done): free the
                     // slot without ordering this thread's pending o stores before it
-                    st_relaxed(&R.freed[k * RING + j % RING], j + 1);
+                    st_relaxed(&((HALF && half) ? R.freed2 : R.freed)[k * RING + j % RING], j + 1);
                     issued_next = false;
                     // with tensor stores of o, the copy goes after MMA1 instead (the
                     // previous chunk's o stores then have had time to read its buffer;
@@ -1241,8 +1249,8 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
                 alive = false;
                 break;
             }
-            if (p.ngate && tid < 2 * BT && (tid >> 1) < nv)  // this chunk's gate rows (two lines each) -> L2
-                prefetch_l2(p.ngate + (static_cast<size_t>(t0 + (tid >> 1)) * p.H + h) * DV + 64 * (tid & 1));
+            if (ngate && tid < 2 * BT && (tid >> 1) < nv)  // this chunk's gate rows (two lines each) -> L2
+                prefetch_l2(ngate + (static_cast<size_t>(t0 + (tid >> 1)) * p.H + h) * DV + 64 * (tid & 1));
             for (int it = 0; !mbar_try_wait(&full[b], (j >> 1) & 1); ++it)
                 if (it > (1 << 20)) {
                     set_status(p.status, KDA_ERR_TIMEOUT);
@@ -1256,7 +1264,7 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
                 const float d = reinterpret_cast<const float *>(bb + SL_D)[row];
                 uint32_t r0[16], r1[16];
                 tmem_ld16(tS, r0);
-                tmem_ld16(tS + 16, r1);
+                if constexpr (NCT > 16) tmem_ld16(tS + 16, r1);
                 tmem_wait_ld();
                 auto snap = [&](uint32_t (&r)[16], int cb) {
                     uint32_t hp[8];
@@ -1266,16 +1274,16 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
                         vmax = max_abs_nan(max_abs_nan(vmax, x0), x1);
                         hp[e] = pack_f16(x0, x1);
                     }
-                    const int c8 = 32 * slice + 16 * cb;
+                    const int c8 = NCT * slice + 16 * cb;
                     *reinterpret_cast<uint4 *>(sS + tile_chunk(128, row, c8)) = make_uint4(hp[0], hp[1], hp[2], hp[3]);
                     *reinterpret_cast<uint4 *>(sS + tile_chunk(128, row, c8 + 8)) = make_uint4(hp[4], hp[5], hp[6], hp[7]);
 #pragma unroll
                     for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * d);
                 };
                 snap(r0, 0);
-                snap(r1, 1);
+                if constexpr (NCT > 16) snap(r1, 1);
                 tmem_st16(tS, r0);
-                tmem_st16(tS + 16, r1);
+                if constexpr (NCT > 16) tmem_st16(tS + 16, r1);
                 tmem_wait_st();
             }
             fence_proxy_async_shared();
@@ -1308,13 +1316,13 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
                 const int t = row - 64;
                 uint32_t r0[16], r1[16];
                 tmem_ld16(tD, r0);
-                tmem_ld16(tD + 16, r1);
+                if constexpr (NCT > 16) tmem_ld16(tD + 16, r1);
                 tmem_wait_ld();
                 auto vnew = [&](const uint32_t (&r)[16], int cb) {
-                    const int c8 = 32 * slice + 16 * cb;
+                    const int c8 = NCT * slice + 16 * cb;  // this CTA's column (u's is v0 + c8)
 #pragma unroll
                     for (int hh = 0; hh < 2; ++hh) {
-                        const uint4 uu = *reinterpret_cast<const uint4 *>(bb + SL_U + tile_chunk(64, t, c8 + 8 * hh));
+                        const uint4 uu = *reinterpret_cast<const uint4 *>(bb + SL_U + tile_chunk(64, t, v0 + c8 + 8 * hh));
                         const uint32_t *uw = reinterpret_cast<const uint32_t *>(&uu);
                         uint32_t vp[4];
 #pragma unroll
@@ -1329,7 +1337,7 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
                     }
                 };
                 vnew(r0, 0);
-                vnew(r1, 1);
+                if constexpr (NCT > 16) vnew(r1, 1);
             }
             fence_proxy_async_shared();
             tc_fence_before();
@@ -1397,11 +1405,11 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
             // the loads land while MMA2/MMA3 run and o is staged.
             static_assert(NCOMP / 32 * 4 == BT, "four output rows per warp");
             uint2 gv[4];
-            if (p.ngate) {
+            if (ngate) {
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) {
                     const int rr = warp + 16 * q4;
-                    gv[q4] = rr < nv ? __ldg(reinterpret_cast<const uint2 *>(p.ngate + (static_cast<size_t>(t0 + rr) * p.H + h) * DV) + lane)
+                    gv[q4] = rr < nv ? __ldg(reinterpret_cast<const uint2 *>(ngate + (static_cast<size_t>(t0 + rr) * p.H + h) * DV) + lane)
                                      : make_uint2(0u, 0u);
                 }
             }
@@ -1414,16 +1422,18 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
                 // [64][32] fp32 boxes, and written by four tensor stores that
                 // run while the next chunk starts (the next copy into this
                 // buffer waits for them to read it).
-                unsigned char *ob = smem + (b ? OFF_BUF1 : OFF_BUF0) + slice * (BT * 128);
+                // (box NCT*slice/32; this thread's first 16-byte chunk in its row: cb0)
+                unsigned char *ob = smem + (b ? OFF_BUF1 : OFF_BUF0) + (NCT * slice / 32) * (BT * 128);
                 if (quad < 2) {
+                    const int cb0 = (NCT * slice % 32) / 4;
                     uint32_t r0[16], r1[16];
                     tmem_ld16(tD, r0);
-                    tmem_ld16(tD + 16, r1);
+                    if constexpr (NCT > 16) tmem_ld16(tD + 16, r1);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int c4 = 0; c4 < 8; ++c4) {
+                    for (int c4 = 0; c4 < NCT / 4; ++c4) {
                         const uint32_t *r = c4 < 4 ? r0 + 4 * c4 : r1 + 4 * (c4 - 4);
-                        *reinterpret_cast<uint4 *>(ob + row * 128 + ((c4 ^ (row & 7)) << 4)) = make_uint4(r[0], r[1], r[2], r[3]);
+                        *reinterpret_cast<uint4 *>(ob + row * 128 + (((cb0 + c4) ^ (row & 7)) << 4)) = make_uint4(r[0], r[1], r[2], r[3]);
                     }
                 }
                 fence_proxy_async_shared();
@@ -1432,7 +1442,7 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
                 if (tid == 0) {
                     const unsigned char *o0 = smem + (b ? OFF_BUF1 : OFF_BUF0);
 #pragma unroll
-                    for (int s4 = 0; s4 < 4; ++s4) tma_store_3d(&p.tm_o, o0 + s4 * (BT * 128), 32 * s4, h, static_cast<int>(t0));
+                    for (int s4 = 0; s4 < NV / 32; ++s4) tma_store_3d(&p.tm_o, o0 + s4 * (BT * 128), v0 + 32 * s4, h, static_cast<int>(t0));
                     bulk_commit();
                 }
                 KDA_TRACE_EV(p, 12, j);
@@ -1449,17 +1459,18 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
             if (quad < 2) {
                 uint32_t r0[16], r1[16];
                 tmem_ld16(tD, r0);
-                tmem_ld16(tD + 16, r1);
+                if constexpr (NCT > 16) tmem_ld16(tD + 16, r1);
                 tmem_wait_ld();
-                float *dst = stg + row * OST + 32 * slice;
+                float *dst = stg + row * OST + NCT * slice;
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     reinterpret_cast<float4 *>(dst)[e] = make_float4(__uint_as_float(r0[4 * e]), __uint_as_float(r0[4 * e + 1]),
                                                                      __uint_as_float(r0[4 * e + 2]), __uint_as_float(r0[4 * e + 3]));
-                    reinterpret_cast<float4 *>(dst + 16)[e] = make_float4(__uint_as_float(r1[4 * e]), __uint_as_float(r1[4 * e + 1]),
-                                                                          __uint_as_float(r1[4 * e + 2]), __uint_as_float(r1[4 * e + 3]));
+                    if constexpr (NCT > 16)
+                        reinterpret_cast<float4 *>(dst + 16)[e] = make_float4(__uint_as_float(r1[4 * e]), __uint_as_float(r1[4 * e + 1]),
+                                                                              __uint_as_float(r1[4 * e + 2]), __uint_as_float(r1[4 * e + 3]));
                 }
-                if (p.ngate) {  // this slice's sum of squares of the row, into the row's pad column 128 + slice
+                if (!HALF && ngate) {  // this slice's sum of squares of the row, into the row's pad column 128 + slice
                     float ss = 0.f;
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
@@ -1474,7 +1485,7 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
             sync_compute();
             if (!p.o) {
                 // states only: no output rows
-            } else if (p.ngate) {
+            } else if (!HALF && ngate) {
                 // y = x / sqrt(mean(x^2) + eps) * weight * sigmoid(gate) over the row's 128 channels
                 const float4 w4 = __ldg(reinterpret_cast<const float4 *>(p.nweight) + lane);
 #pragma unroll
@@ -1493,8 +1504,9 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
                 }
             } else {
                 for (int rr = warp; rr < nv; rr += NCOMP / 32)
-                    reinterpret_cast<float4 *>(p.o + (static_cast<size_t>(t0 + rr) * p.H + h) * DV)[lane] =
-                        *reinterpret_cast<const float4 *>(stg + rr * OST + 4 * lane);
+                    if (NV == 128 || lane < NV / 4)
+                        reinterpret_cast<float4 *>(p.o + (static_cast<size_t>(t0 + rr) * p.H + h) * DV + v0)[lane] =
+                            *reinterpret_cast<const float4 *>(stg + rr * OST + 4 * lane);
             }
             KDA_TRACE_EV(p, 12, j);
             if (tid == 0 && !issued_next && j + 1 < total) {
@@ -1511,11 +1523,11 @@ __device__ __forceinline__ void run(const Params &p, unsigned char *smem, int k)
         if (p.sT && st_inb) {
             tc_fence_after();
 #pragma unroll
-            for (int cb = 0; cb < 2; ++cb) {
+            for (int cb = 0; cb < NCT / 16; ++cb) {
                 uint32_t r[16];
                 tmem_ld16(tS + 16 * cb, r);
                 tmem_wait_ld();
-                float4 *dst = reinterpret_cast<float4 *>(p.sT + state_base + row * DV + 32 * slice + 16 * cb);
+                float4 *dst = reinterpret_cast<float4 *>(p.sT + state_base + row * DV + v0 + NCT * slice + 16 * cb);
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
                     dst[e] = make_float4(__uint_as_float(r[4 * e]), __uint_as_float(r[4 * e + 1]),
@@ -1543,7 +1555,7 @@ constexpr int SMEM_MAX = SMEM_TILES;
 #endif
 static_assert(SMEM_MAX <= 232448, "shared memory budget");
 
-template <bool WY>  // the consumers form the WY product
+template <bool WY, bool HALF>  // the consumers form the WY product; consumers are CTA pairs
 __global__ void __launch_bounds__(NTHREADS, 1) kda_persistent_kernel(const __grid_constant__ Params p) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -1552,10 +1564,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_persistent_kernel(const __gri
     __syncthreads();
 #endif
     build_sched(p, smem + OFF_SCHED, smem);  // the roles' tiles serve as scratch until it returns
-    if (static_cast<int>(blockIdx.x) < p.C)
-        cons::run<WY>(p, smem, blockIdx.x);
+    // consumer CTAs first: with HALF, CTA k and k + C are the two column halves of consumer k
+    const int ncons = HALF ? 2 * p.C : p.C;
+    if (static_cast<int>(blockIdx.x) < ncons)
+        cons::run<WY, HALF>(p, smem, HALF ? static_cast<int>(blockIdx.x) % p.C : static_cast<int>(blockIdx.x),
+                            HALF ? static_cast<int>(blockIdx.x) / p.C : 0);
     else
-        prod::run<WY>(p, smem, blockIdx.x - p.C);
+        prod::run<WY, HALF>(p, smem, blockIdx.x - ncons);
 }
 
 // ------------------------------------------------------------------ host side
@@ -1655,6 +1670,23 @@ bool wy_for(int64_t chains, int64_t tokens, int64_t seqs, int C, int grid) {
     return t_cons < t_prod;
 }
 
+// Whether each chain's 128 value columns go to a pair of consumer CTAs, one
+// column half each (the consumer's MMAs, epilogues and state then halve; both
+// CTAs copy the whole slot). Only where every chain can have a pair within half
+// the SMs, by the estimate of consumers_for with a split consumer chunk at
+// about 2.6 us against 3.5, and the producers short of the second CTAs.
+bool split_for(int64_t chains, int64_t tokens, int64_t seqs, int C, int grid) {
+    if (chains < 1 || seqs < 1 || C < 1 || C >= grid || 2 * chains > grid / 2) return false;
+    constexpr double T_CONS = 3.5, T_SPLIT = 2.6, T_PROD = 7.0;
+    const double chunks = static_cast<double>(chains / seqs) *
+                          (static_cast<double>(tokens) / BT + 0.5 * static_cast<double>(seqs));
+    const double per_chain = chunks / static_cast<double>(chains);
+    const double whole = std::fmax(static_cast<double>((chains + C - 1) / C) * per_chain * T_CONS,
+                                   chunks * T_PROD / static_cast<double>(grid - C));
+    const double split = std::fmax(per_chain * T_SPLIT, chunks * T_PROD / static_cast<double>(grid - 2 * chains));
+    return split < whole;
+}
+
 size_t workspace_bytes(int64_t chains) {
     const int sms = num_sms();
     if (sms < 2 || chains < 1) return 0;
@@ -1672,6 +1704,7 @@ cudaError_t launch(Params p, size_t ws_bytes, cudaStream_t stream) {
     const int grid = sms;  // one CTA per SM; all co-resident (cooperative launch)
     const int64_t chains = static_cast<int64_t>(p.N) * p.H;
     p.C = consumers_for(chains, p.T, p.N, grid);
+    p.CH = 1;
     p.Cws = max_consumers(chains, grid);
     p.spin = (p.debug & KDA_DEBUG_WITHHOLD_READY) ? SPIN_LIMIT_DEBUG : SPIN_LIMIT;
     if (ws_bytes < ring_offset(p.Cws) + static_cast<size_t>(p.Cws) * RING * SLOT_BYTES) return cudaErrorInvalidValue;
@@ -1684,13 +1717,23 @@ cudaError_t launch(Params p, size_t ws_bytes, cudaStream_t stream) {
         (void)cudaGetLastError();  // clear a failed query
     }
     p.o_tma = (o_device && !p.ngate && encode_o(&p.tm_o, p.o, p.Ttok, p.H)) ? 1 : 0;
+    // a chain's columns split over two consumer CTAs (not with the gated norm,
+    // which needs whole rows of o, nor with the consumers' WY form)
+    bool split = !p.ngate && split_for(chains, p.T, p.N, p.C, grid);
+    if (p.debug & KDA_DEBUG_SPLIT_COLUMNS) split = !p.ngate && 2 * chains <= grid / 2;
+    if (p.debug & (KDA_DEBUG_WHOLE_COLUMNS | KDA_DEBUG_WY_CONSUMER)) split = false;
+    if (split) {
+        p.C = static_cast<int32_t>(chains);
+        p.CH = 2;
+    }
     // the consumers take the WY product only with o on tensor stores (the
     // warps' own o stores, and the gated norm, leave them no slack for it)
-    bool wy = p.o_tma && wy_for(chains, p.T, p.N, p.C, grid);
+    bool wy = !split && p.o_tma && wy_for(chains, p.T, p.N, p.C, grid);
     if (p.debug & KDA_DEBUG_WY_PRODUCER) wy = false;
     if (p.debug & KDA_DEBUG_WY_CONSUMER) wy = true;
-    const void *kernel = wy ? reinterpret_cast<const void *>(kda_persistent_kernel<true>)
-                            : reinterpret_cast<const void *>(kda_persistent_kernel<false>);
+    const void *kernel = split ? reinterpret_cast<const void *>(kda_persistent_kernel<false, true>)
+                         : wy  ? reinterpret_cast<const void *>(kda_persistent_kernel<true, false>)
+                               : reinterpret_cast<const void *>(kda_persistent_kernel<false, false>);
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_MAX);
     if (e != cudaSuccess) return e;
     int per_sm = 0;

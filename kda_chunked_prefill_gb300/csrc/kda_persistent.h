@@ -24,7 +24,9 @@ struct Params {
     float *o, *sT;       // o may be NULL (nothing written but the final states)
     int32_t *status;
     unsigned char *ws;
-    int32_t C;           // consumer CTAs (set by launch)
+    int32_t C;           // ring consumers (set by launch): chains go to them, tasks are numbered by them
+    int32_t CH;          // consumer CTAs per ring consumer (set by launch): 2 when the 128 value
+                         // columns of a chain are split over two CTAs, else 1
     int32_t Cws;         // consumers the workspace rings were sized for (>= C)
     uint32_t debug;      // KDA_DEBUG_* flags (0 in normal calls)
     int32_t raw;         // 1: g and beta are raw (activated in the producer), see kda_chunk_fwd_raw_gates
@@ -44,14 +46,16 @@ struct Params {
     CUtensorMap tm_o;
 };
 
-// workspace: [64-byte header][ready C*RING][freed C*RING] padded to 1024, then the slots
+// workspace: [64-byte header][ready C*RING][freed C*RING][freed by the second column half
+// C*RING] padded to 1024, then the slots
 __host__ __device__ constexpr size_t ring_offset(int C) {
-    return ((64 + 8 * static_cast<size_t>(C) * RING) + 1023) / 1024 * 1024;
+    return ((64 + 12 * static_cast<size_t>(C) * RING) + 1023) / 1024 * 1024;
 }
 
 int max_consumers(int64_t chains, int grid);
 int consumers_for(int64_t chains, int64_t tokens, int64_t seqs, int grid);
 bool wy_for(int64_t chains, int64_t tokens, int64_t seqs, int C, int grid);
+bool split_for(int64_t chains, int64_t tokens, int64_t seqs, int C, int grid);
 size_t workspace_bytes(int64_t chains);
 cudaError_t launch(Params p, size_t ws_bytes, cudaStream_t stream);
 

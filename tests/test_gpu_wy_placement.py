@@ -44,5 +44,5 @@ def test_plan_on_this_device():
     # num_sms = 0 asks the current device; on it, the plan is the one for its SM count
     import torch
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    for shape in ((4, 8192, 16), (1, 16384, 96), (16, 12091, 16)):
+    for shape in ((4, 8192, 16), (1, 16384, 96), (16, 12091, 16), (1, 65536, 4)):
         assert kda.chunk_fwd_plan(*shape) == kda.chunk_fwd_plan(*shape, num_sms=sms)

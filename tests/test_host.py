@@ -101,15 +101,19 @@ def _call_debug(lib, flags, **over):
 
 
 def test_debug_entry_rejects_unknown_flags(lib):
-    assert _call_debug(lib, 8) == kda.KDA_ERR_INVALID_ARG
+    assert _call_debug(lib, 32) == kda.KDA_ERR_INVALID_ARG
     assert _call_debug(lib, 0x80000001) == kda.KDA_ERR_INVALID_ARG
     # the two WY placements exclude each other
     assert _call_debug(lib, kda.KDA_DEBUG_WY_PRODUCER | kda.KDA_DEBUG_WY_CONSUMER) == kda.KDA_ERR_INVALID_ARG
+    # nor do the two column layouts, or split columns with the consumers' WY form
+    assert _call_debug(lib, kda.KDA_DEBUG_SPLIT_COLUMNS | kda.KDA_DEBUG_WHOLE_COLUMNS) == kda.KDA_ERR_INVALID_ARG
+    assert _call_debug(lib, kda.KDA_DEBUG_SPLIT_COLUMNS | kda.KDA_DEBUG_WY_CONSUMER) == kda.KDA_ERR_INVALID_ARG
 
 
 def test_debug_entry_accepts_each_wy_placement(lib):
     for flags in (kda.KDA_DEBUG_WY_PRODUCER, kda.KDA_DEBUG_WY_CONSUMER,
-                  kda.KDA_DEBUG_WY_CONSUMER | kda.KDA_DEBUG_WITHHOLD_READY):
+                  kda.KDA_DEBUG_WY_CONSUMER | kda.KDA_DEBUG_WITHHOLD_READY, kda.KDA_DEBUG_SPLIT_COLUMNS,
+                  kda.KDA_DEBUG_WHOLE_COLUMNS | kda.KDA_DEBUG_WY_PRODUCER):
         # validation runs first: a bad head size is still refused as such, and an empty call succeeds
         assert _call_debug(lib, flags, dk=64) == kda.KDA_ERR_UNSUPPORTED
         assert _call_debug(lib, flags, N=0, T=0, q=None, k=None, v=None, g=None,
@@ -304,29 +308,32 @@ def test_empty_problem_is_a_no_op(lib):
     assert kda.chunk_fwd_launches(4, 8192, 16) == 1
 
 
-# ---- kda_chunk_fwd_plan: the launch's two choices, on the host
+# ---- kda_chunk_fwd_plan: the launch's choices, on the host
 @pytest.mark.parametrize("shape,sms,plain,expect", [
-    ((4, 8192, 16), 152, True, (64, True)),     # the equal-length batch: consumers have slack
-    ((4, 8192, 16), 152, False, (64, False)),   # o not on tensor stores: the producers keep it
-    ((1, 16384, 96), 152, True, (48, False)),   # two chains per consumer: consumer-bound
-    ((3, 24576, 96), 152, True, (48, False)),
-    ((1, 65536, 4), 152, True, (4, False)),     # few long chains
-    ((4, 4390, 16), 152, True, (64, False)),    # lengths cannot all be equal
-    ((16, 12091, 16), 152, True, (52, False)),
-    ((1, 256, 2), 152, True, (2, False)),
+    ((4, 8192, 16), 152, True, (64, True, False)),    # the equal-length batch: consumers have slack
+    ((4, 8192, 16), 152, False, (64, False, False)),  # o not on tensor stores: the producers keep it
+    ((1, 16384, 96), 152, True, (48, False, False)),  # two chains per consumer: consumer-bound
+    ((3, 24576, 96), 152, True, (48, False, False)),
+    ((4, 4390, 16), 152, True, (64, False, False)),   # lengths cannot all be equal
+    ((16, 12091, 16), 152, True, (52, False, False)),
+    ((1, 65536, 4), 152, True, (4, False, True)),     # few long chains: columns split over CTA pairs
+    ((1, 723, 16), 152, True, (16, False, True)),
+    ((2, 923, 16), 152, True, (32, False, True)),     # 64 consumer CTAs: still within half the SMs
+    ((1, 256, 2), 152, True, (2, False, True)),
 ])
 def test_plan_matches_the_launch_rule(lib, shape, sms, plain, expect):
     assert kda.chunk_fwd_plan(*shape, num_sms=sms, plain_device_o=plain) == expect
 
 
 def test_plan_rejects_bad_arguments(lib):
-    c, w = ctypes.c_int32(0), ctypes.c_int32(0)
-    ok = (ctypes.byref(c), ctypes.byref(w))
+    c, w, sp = ctypes.c_int32(0), ctypes.c_int32(0), ctypes.c_int32(0)
+    ok = (ctypes.byref(c), ctypes.byref(w), ctypes.byref(sp))
     assert lib.kda_chunk_fwd_plan(0, 100, 4, 152, 1, *ok) == kda.KDA_ERR_INVALID_ARG
     assert lib.kda_chunk_fwd_plan(2, 100, 0, 152, 1, *ok) == kda.KDA_ERR_INVALID_ARG
     assert lib.kda_chunk_fwd_plan(2, -1, 4, 152, 1, *ok) == kda.KDA_ERR_INVALID_ARG
     assert lib.kda_chunk_fwd_plan(2, 100, 4, -1, 1, *ok) == kda.KDA_ERR_INVALID_ARG
-    assert lib.kda_chunk_fwd_plan(2, 100, 4, 152, 1, None, ctypes.byref(w)) == kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_chunk_fwd_plan(2, 100, 4, 152, 1, None, ctypes.byref(w), ctypes.byref(sp)) == kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_chunk_fwd_plan(2, 100, 4, 152, 1, ctypes.byref(c), ctypes.byref(w), None) == kda.KDA_ERR_INVALID_ARG
     assert lib.kda_chunk_fwd_plan(2, 100, 4, 1, 1, *ok) == kda.KDA_ERR_UNSUPPORTED
     import torch
     if not torch.cuda.is_available():  # the current device is asked for its SM count
